@@ -1,0 +1,172 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MegaMoE expert layer.
+ *
+ * One call of moe_forward runs, on the caller's CUDA stream, the whole expert
+ * layer of a Mixture-of-Experts block on one GPU:
+ *
+ *   1. dispatch: per-expert counts, exclusive prefix, stable gather map
+ *      (MegaMoE SM90 Implementation Design (Final), §9.2; PR357 Green-Context
+ *      Split MegaMoE code review, §6.1);
+ *   2. L1 grouped GEMM x . W1^T with block scales applied per 128-K block
+ *      (design §5.2-§5.3);
+ *   3. SwiGLU silu(gate) * up, times the top-k weight (design §10.1 steps 1-3);
+ *   4. per-row, per-64-column FP8 E4M3 requantisation, sf = amax / 448
+ *      (design §10.1 steps 4-6, §1.1 decision 9);
+ *   5. L2 grouped GEMM with the two per-64 activation scales of every
+ *      128-K block (design §5.4);
+ *   6. BF16 rounding of each (token, slot) output (design §11.1);
+ *   7. top-k combine: FP32 sum over active slots in slot order, BF16 y
+ *      (design §11.2; PR357 review §6.3 "K3 combine_reduce").
+ *
+ * Pointers: every buffer argument of moe_create / moe_transform_weights /
+ * moe_forward / moe_get_* is DEVICE memory owned by the caller, except the
+ * h_* arguments of moe_forward_host, which are HOST memory.  The library never
+ * allocates device memory: the caller passes a workspace of
+ * moe_workspace_bytes() bytes and a weight store of moe_weight_bytes() bytes,
+ * both 256-byte aligned, which must outlive the context.  A moe_ctx holds
+ * host state only.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Calls are stream-ordered and asynchronous unless stated otherwise; two
+ * forwards of one context must not run concurrently (they share the
+ * workspace).  Back-to-back forwards need no reset by the caller.
+ *
+ * Errors: every int-returning call returns MOE_OK (0) or a negative MOE_ERR_*
+ * code; nothing is thrown across the ABI.  Argument and shape errors are
+ * detected on the host before anything is launched.  Faults found on the
+ * device (an expert id outside [-1, E), a pipeline wait that timed out) are
+ * recorded in a device error word that moe_device_status() reads.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)    /* null pointer, bad size, misaligned buffer */
+#define MOE_ERR_UNSUPPORTED (-2)    /* shape or format this build does not run */
+#define MOE_ERR_CUDA (-3)           /* a CUDA runtime/driver call failed */
+#define MOE_ERR_DEVICE_TIMEOUT (-4) /* a bounded device-side wait gave up */
+#define MOE_ERR_BAD_EXPERT (-5)     /* topk_idx held an id outside [-1, E) */
+#define MOE_ERR_NOT_READY (-6)      /* moe_forward before moe_transform_weights */
+
+typedef struct moe_ctx moe_ctx;
+
+/* Weight formats.
+ * MOE_W_FP8_BLK128: W1/W2 FP8 E4M3 with one f32 scale per 128x128 block,
+ *   activations x FP8 E4M3 with one f32 scale per 1x128 (recipe (1,1,128),
+ *   design §16.1 and §15.2).
+ * MOE_W_FP4_E2M1_UE8M0_32: W1/W2 FP4 E2M1 (two codes per byte, low nibble =
+ *   even k) with one UE8M0 scale per 1x32; activations FP8 E4M3 with one UE8M0
+ *   scale per 1x32 (design §2.1, PR357 review §1).  Not yet run by this
+ *   build: moe_create returns MOE_ERR_UNSUPPORTED. */
+typedef enum { MOE_W_FP8_BLK128 = 0, MOE_W_FP4_E2M1_UE8M0_32 = 1 } moe_wfmt;
+
+typedef struct {
+    int max_tokens;   /* T_max: largest num_tokens a forward may pass (>= 1) */
+    int hidden;       /* H, multiple of 128 */
+    int inter;        /* I (intermediate size per expert), multiple of 128 */
+    int num_experts;  /* E, 1..1024 */
+    int topk;         /* k, 1..32 */
+    int wfmt;         /* moe_wfmt */
+    float act_clamp;  /* symmetric clamp of gate and up before SwiGLU; +INFINITY = off
+                         (design §10.1 step 3, §1.1 decision 16) */
+    int fast_math;    /* 0: expf and IEEE division in SwiGLU; 1: __expf / fast divide */
+} moe_config;
+
+/* Bytes of device workspace / transformed-weight storage for `cfg`
+ * (0 if `cfg` is invalid). */
+MOE_API size_t moe_workspace_bytes(const moe_config *cfg);
+MOE_API size_t moe_weight_bytes(const moe_config *cfg);
+
+/* Create a context bound to the current CUDA device.  d_workspace and
+ * d_weights are caller-owned device buffers of the sizes above (256-byte
+ * aligned).  Writes *out on success. */
+MOE_API int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_weights);
+
+/* Read the canonical weights and write the kernel layout into d_weights
+ * (design §15: gate/up rows interleaved in groups of 8 along N).
+ * Canonical layouts, all row-major (MOE_W_FP8_BLK128):
+ *   w1    u8 (E4M3) [E, 2I, H]    rows [0, I) = gate, rows [I, 2I) = up
+ *   w1_sf f32       [E, 2I/128, H/128]
+ *   w2    u8 (E4M3) [E, H, I]
+ *   w2_sf f32       [E, H/128, I/128]
+ * The inputs may be freed once the stream has passed this call. */
+MOE_API int moe_transform_weights(moe_ctx *ctx, const void *w1, const void *w1_sf,
+                          const void *w2, const void *w2_sf, void *stream);
+
+/* One forward pass (design §3.3).
+ *   num_tokens T, 0 <= T <= max_tokens (T = 0 returns at once)
+ *   x             u8 (E4M3) [T, H] row-major, rows 16-byte aligned
+ *   x_sf          f32 [T, H/128]
+ *   topk_idx      int32 [T, k]; -1 marks an inactive slot
+ *   topk_weights  f32 [T, k]
+ *   y             bf16 [T, H] (written)
+ *   cumulative_expert_counts  int32 [E] or NULL: the per-expert counts of
+ *                 this call are added to it (design §16.1
+ *                 "cumulative_local_expert_recv_stats")
+ * Asynchronous on `stream`. */
+MOE_API int moe_forward(moe_ctx *ctx, int num_tokens, const void *x, const void *x_sf,
+                const int32_t *topk_idx, const float *topk_weights, void *y,
+                int32_t *cumulative_expert_counts, void *stream);
+
+/* moe_forward with HOST inputs and output: copies h_x, h_x_sf, h_topk_idx,
+ * h_topk_weights into the workspace, runs the forward and copies y back to
+ * h_y, then synchronises `stream`.  Host buffers may be pageable or pinned
+ * (pinned is faster). */
+MOE_API int moe_forward_host(moe_ctx *ctx, int num_tokens, const void *h_x, const void *h_x_sf,
+                     const int32_t *h_topk_idx, const float *h_topk_weights, void *h_y,
+                     void *stream);
+
+/* Copy the dispatch result of the last forward (T tokens) into caller device
+ * buffers: counts int32 [E], offsets int32 [E+1] (exclusive prefix of
+ * counts), gather int32 [T*k] whose first offsets[E] entries are the pair ids
+ * t*k + j of each expert's pairs in (token, slot) order, experts ascending
+ * (later entries unspecified).  Any pointer may be NULL. */
+MOE_API int moe_get_dispatch(moe_ctx *ctx, int32_t *counts, int32_t *offsets, int32_t *gather,
+                     void *stream);
+
+/* Copy intermediates of the last forward (T tokens; row r belongs to pair
+ * gather[r], rows r >= offsets[E] unspecified), P = T*k:
+ * l2_acts u8 (E4M3) [P, I], l2_sf f32 [I/64, P] (the L2 activation scales),
+ * l2_out bf16 [P, H] (the rounded L2 outputs).  Any pointer may be NULL.
+ * For stage-by-stage tests. */
+MOE_API int moe_get_intermediates(moe_ctx *ctx, void *l2_acts, float *l2_sf, void *l2_out,
+                          void *stream);
+
+/* Per-stage timing of the next `max_forwards` forwards: moe_profile_begin
+ * creates CUDA events (no device memory) and every following moe_forward
+ * records one event before its dispatch and one after each of its four
+ * stages (dispatch, L1 GEMM, L2 GEMM, combine) on its stream.
+ * moe_profile_end synchronises those events, writes the summed milliseconds
+ * of each stage to stage_ms[4] and the number of recorded forwards to
+ * *n_forwards, and releases the events. */
+MOE_API int moe_profile_begin(moe_ctx *ctx, int max_forwards);
+MOE_API int moe_profile_end(moe_ctx *ctx, float *stage_ms, int *n_forwards);
+
+/* Synchronise the device, read and clear the device error word:
+ * MOE_OK, MOE_ERR_BAD_EXPERT, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_CUDA. */
+MOE_API int moe_device_status(moe_ctx *ctx);
+
+/* Static description of an error code. */
+MOE_API const char *moe_strerror(int code);
+
+/* Free the host state (never the caller's buffers). NULL is allowed. */
+MOE_API void moe_destroy(moe_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

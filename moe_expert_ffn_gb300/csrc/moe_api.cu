@@ -1,0 +1,412 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: workspace carving, TMA
+// tensor maps, argument checks and the launch sequence of one forward
+// (dispatch -> L1 GEMM -> L2 GEMM -> combine) on the caller's stream.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "moe.h"
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    // workspace
+    size_t err, count, offset, mb_prefix, mblk_expert, gather, pair_pool;
+    size_t l2_acts, l2_sf, l2_out;
+    size_t st_x, st_xsf, st_idx, st_w, st_y;
+    size_t ws_total;
+    // weights
+    size_t w1i, w1i_sf, w2, w2_sf;
+    size_t wt_total;
+};
+
+bool valid_cfg(const moe_config *c) {
+    if (!c) return false;
+    if (c->max_tokens < 1 || c->hidden < 128 || c->inter < 128) return false;
+    if (c->hidden % 128 || c->inter % 128) return false;
+    if (c->num_experts < 1 || c->num_experts > 1024) return false;
+    if (c->topk < 1 || c->topk > 32 || c->topk > c->num_experts) return false;
+    if (c->wfmt != MOE_W_FP8_BLK128 && c->wfmt != MOE_W_FP4_E2M1_UE8M0_32) return false;
+    if (isnan(c->act_clamp) || c->act_clamp <= 0.0f) return false;
+    const long long pm = (long long)c->max_tokens * c->topk;
+    if (pm > (1ll << 24)) return false;
+    if ((long long)c->num_experts * 2 * c->inter >= (1ll << 31)) return false;
+    if ((long long)c->num_experts * c->hidden >= (1ll << 31)) return false;
+    return true;
+}
+
+Layout make_layout(const moe_config *c) {
+    Layout L;
+    const size_t Tm = c->max_tokens, k = c->topk, E = c->num_experts, H = c->hidden, I = c->inter;
+    const size_t Pm = Tm * k;
+    const size_t MBmax = Pm / kBM + E + 1;
+    size_t o = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        o = align_up(o, align);
+        const size_t at = o;
+        o += bytes;
+        return at;
+    };
+    L.err = take(sizeof(int) * 4, 256);
+    L.count = take(4 * E, 256);
+    L.offset = take(4 * (E + 1), 256);
+    L.mb_prefix = take(4 * (E + 1), 256);
+    L.mblk_expert = take(4 * MBmax, 256);
+    L.gather = take(4 * Pm, 256);
+    L.pair_pool = take(4 * Pm, 256);
+    L.l2_acts = take(Pm * I, kAlign);
+    L.l2_sf = take(4 * (I / 64) * Pm, kAlign);
+    L.l2_out = take(2 * Pm * H, kAlign);
+    L.st_x = take(Tm * H, kAlign);
+    L.st_xsf = take(4 * Tm * (H / 128), 256);
+    L.st_idx = take(4 * Tm * k, 256);
+    L.st_w = take(4 * Tm * k, 256);
+    L.st_y = take(2 * Tm * H, kAlign);
+    L.ws_total = align_up(o, kAlign);
+
+    o = 0;
+    L.w1i = take(E * 2 * I * H, kAlign);
+    L.w1i_sf = take(8 * E * (2 * I / 128) * (H / 128), 256);
+    L.w2 = take(E * H * I, kAlign);
+    L.w2_sf = take(4 * E * (H / 128) * (I / 128), 256);
+    L.wt_total = align_up(o, kAlign);
+    return L;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D byte tensor [outer, inner] with row stride `stride` bytes, boxes of
+// box_inner x box_outer, 128-byte swizzle (box_inner must be 128).
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
+              uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct moe_ctx {
+    moe_config cfg;
+    Layout L;
+    int device;
+    int num_sms;
+    uint8_t *ws;
+    uint8_t *wt;
+    bool weights_ready;
+    int last_T;
+    CUtensorMap tm_w1, tm_w2, tm_l2a;
+    cudaEvent_t *prof_ev;   // 5 events per profiled forward
+    int prof_max, prof_n;
+
+    template <class T>
+    T *w(size_t off) const { return reinterpret_cast<T *>(ws + off); }
+    template <class T>
+    T *wt_at(size_t off) const { return reinterpret_cast<T *>(wt + off); }
+};
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config *cfg) {
+    if (!valid_cfg(cfg)) return 0;
+    return make_layout(cfg).ws_total;
+}
+
+size_t moe_weight_bytes(const moe_config *cfg) {
+    if (!valid_cfg(cfg)) return 0;
+    return make_layout(cfg).wt_total;
+}
+
+int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_weights) {
+    if (!out || !valid_cfg(cfg) || !d_workspace || !d_weights) return MOE_ERR_INVALID_ARG;
+    if (!aligned(d_workspace, 256) || !aligned(d_weights, 256)) return MOE_ERR_INVALID_ARG;
+    if (cfg->wfmt != MOE_W_FP8_BLK128) return MOE_ERR_UNSUPPORTED;
+    moe_ctx *c = static_cast<moe_ctx *>(calloc(1, sizeof(moe_ctx)));
+    if (!c) return MOE_ERR_INVALID_ARG;
+    c->cfg = *cfg;
+    c->L = make_layout(cfg);
+    c->ws = static_cast<uint8_t *>(d_workspace);
+    c->wt = static_cast<uint8_t *>(d_weights);
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+        free(c);
+        return MOE_ERR_CUDA;
+    }
+    const moe_config &g = c->cfg;
+    const uint64_t E = g.num_experts, H = g.hidden, I = g.inter;
+    const uint64_t Pm = (uint64_t)g.max_tokens * g.topk;
+    bool ok = make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
+              make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128) &&
+              make_map(&c->tm_l2a, c->ws + c->L.l2_acts, I, Pm, I, 128, 128);
+    if (!ok) {
+        free(c);
+        return MOE_ERR_CUDA;
+    }
+    // zero the error word
+    if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * 4) != cudaSuccess) {
+        free(c);
+        return MOE_ERR_CUDA;
+    }
+    *out = c;
+    return MOE_OK;
+}
+
+int moe_transform_weights(moe_ctx *c, const void *w1, const void *w1_sf, const void *w2,
+                          const void *w2_sf, void *stream) {
+    if (!c || !w1 || !w1_sf || !w2 || !w2_sf) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w1, 16) || !aligned(w2, 16) || !aligned(w1_sf, 4) || !aligned(w2_sf, 4))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const moe_config &g = c->cfg;
+    const size_t E = g.num_experts, H = g.hidden, I = g.inter;
+    launch_transform_w1(static_cast<const uint8_t *>(w1), static_cast<const float *>(w1_sf),
+                        c->wt_at<uint8_t>(c->L.w1i), c->wt_at<float2>(c->L.w1i_sf), (int)E, (int)H,
+                        (int)I, s);
+    if (cudaMemcpyAsync(c->wt + c->L.w2, w2, E * H * I, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(c->wt + c->L.w2_sf, w2_sf, 4 * E * (H / 128) * (I / 128),
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    c->weights_ready = true;
+    return MOE_OK;
+}
+
+int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_t *topk_idx,
+                const float *topk_weights, void *y, int32_t *stats, void *stream) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    const moe_config &g = c->cfg;
+    if (T < 0 || T > g.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (!c->weights_ready) return MOE_ERR_NOT_READY;
+    if (T == 0) return MOE_OK;
+    if (!x || !x_sf || !topk_idx || !topk_weights || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(x_sf, 4) || !aligned(topk_idx, 4) ||
+        !aligned(topk_weights, 4) || (stats && !aligned(stats, 4)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int E = g.num_experts, H = g.hidden, I = g.inter, k = g.topk;
+    const int Pm = g.max_tokens * k;
+    const Layout &L = c->L;
+
+    DispatchOut o;
+    o.count = c->w<int32_t>(L.count);
+    o.offset = c->w<int32_t>(L.offset);
+    o.mb_prefix = c->w<int32_t>(L.mb_prefix);
+    o.mblk_expert = c->w<int32_t>(L.mblk_expert);
+    o.gather = c->w<int32_t>(L.gather);
+    o.pair_pool = c->w<int32_t>(L.pair_pool);
+    o.stats = stats;
+    o.err = c->w<int>(L.err);
+    cudaEvent_t *ev = (c->prof_ev && c->prof_n < c->prof_max) ? c->prof_ev + 5 * c->prof_n++ : nullptr;
+    if (ev) cudaEventRecord(ev[0], s);
+    launch_dispatch(topk_idx, T, k, E, o, s);
+    if (ev) cudaEventRecord(ev[1], s);
+
+    CUtensorMap tm_x;
+    if (!make_map(&tm_x, x, (uint64_t)H, (uint64_t)T, (uint64_t)H, 128, 1)) return MOE_ERR_CUDA;
+
+    L1Params p1;
+    p1.gather = o.gather;
+    p1.offset = o.offset;
+    p1.mb_prefix = o.mb_prefix;
+    p1.mblk_expert = o.mblk_expert;
+    p1.x_sf = static_cast<const float *>(x_sf);
+    p1.topk_w = topk_weights;
+    p1.w1_sf = c->wt_at<float2>(L.w1i_sf);
+    p1.l2_acts = c->w<uint8_t>(L.l2_acts);
+    p1.l2_sf = c->w<float>(L.l2_sf);
+    p1.err = o.err;
+    p1.H = H;
+    p1.I = I;
+    p1.E = E;
+    p1.k = k;
+    p1.Pmax = Pm;
+    p1.clamp = g.act_clamp;
+    launch_l1(tm_x, c->tm_w1, p1, g.fast_math, c->num_sms, s);
+    if (ev) cudaEventRecord(ev[2], s);
+
+    L2Params p2;
+    p2.offset = o.offset;
+    p2.mb_prefix = o.mb_prefix;
+    p2.mblk_expert = o.mblk_expert;
+    p2.l2_sf = p1.l2_sf;
+    p2.w2_sf = c->wt_at<float>(L.w2_sf);
+    p2.l2_out = c->w<uint16_t>(L.l2_out);
+    p2.err = o.err;
+    p2.H = H;
+    p2.I = I;
+    p2.E = E;
+    p2.Pmax = Pm;
+    launch_l2(c->tm_l2a, c->tm_w2, p2, c->num_sms, s);
+    if (ev) cudaEventRecord(ev[3], s);
+
+    launch_combine(p2.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);
+    if (ev) cudaEventRecord(ev[4], s);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    c->last_T = T;
+    return MOE_OK;
+}
+
+int moe_forward_host(moe_ctx *c, int T, const void *h_x, const void *h_x_sf,
+                     const int32_t *h_topk_idx, const float *h_topk_weights, void *h_y,
+                     void *stream) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    const moe_config &g = c->cfg;
+    if (T < 0 || T > g.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (!c->weights_ready) return MOE_ERR_NOT_READY;
+    if (T == 0) return MOE_OK;
+    if (!h_x || !h_x_sf || !h_topk_idx || !h_topk_weights || !h_y) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t H = g.hidden, k = g.topk;
+    const Layout &L = c->L;
+    if (cudaMemcpyAsync(c->ws + L.st_x, h_x, (size_t)T * H, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(c->ws + L.st_xsf, h_x_sf, (size_t)T * (H / 128) * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(c->ws + L.st_idx, h_topk_idx, (size_t)T * k * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(c->ws + L.st_w, h_topk_weights, (size_t)T * k * 4, cudaMemcpyHostToDevice, s))
+        return MOE_ERR_CUDA;
+    int r = moe_forward(c, T, c->ws + L.st_x, c->ws + L.st_xsf, c->w<int32_t>(L.st_idx),
+                        c->w<float>(L.st_w), c->ws + L.st_y, nullptr, stream);
+    if (r != MOE_OK) return r;
+    if (cudaMemcpyAsync(h_y, c->ws + L.st_y, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s) ||
+        cudaStreamSynchronize(s))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_get_dispatch(moe_ctx *c, int32_t *counts, int32_t *offsets, int32_t *gather, void *stream) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t E = c->cfg.num_experts, P = (size_t)c->last_T * c->cfg.topk;
+    if (counts && cudaMemcpyAsync(counts, c->ws + c->L.count, 4 * E, cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    if (offsets && cudaMemcpyAsync(offsets, c->ws + c->L.offset, 4 * (E + 1), cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    if (gather && P && cudaMemcpyAsync(gather, c->ws + c->L.gather, 4 * P, cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_get_intermediates(moe_ctx *c, void *l2_acts, float *l2_sf, void *l2_out, void *stream) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t H = c->cfg.hidden, I = c->cfg.inter;
+    const size_t P = (size_t)c->last_T * c->cfg.topk;
+    const size_t Pm = (size_t)c->cfg.max_tokens * c->cfg.topk;
+    if (!P) return MOE_OK;
+    if (l2_acts && cudaMemcpyAsync(l2_acts, c->ws + c->L.l2_acts, P * I, cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    if (l2_sf && cudaMemcpy2DAsync(l2_sf, P * 4, c->ws + c->L.l2_sf, Pm * 4, P * 4, I / 64,
+                                   cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    if (l2_out && cudaMemcpyAsync(l2_out, c->ws + c->L.l2_out, P * H * 2, cudaMemcpyDeviceToDevice, s))
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+static void profile_release(moe_ctx *c) {
+    if (!c->prof_ev) return;
+    for (int i = 0; i < 5 * c->prof_max; ++i) cudaEventDestroy(c->prof_ev[i]);
+    free(c->prof_ev);
+    c->prof_ev = nullptr;
+    c->prof_max = c->prof_n = 0;
+}
+
+int moe_profile_begin(moe_ctx *c, int max_forwards) {
+    if (!c || max_forwards < 1 || max_forwards > 100000) return MOE_ERR_INVALID_ARG;
+    profile_release(c);
+    c->prof_ev = static_cast<cudaEvent_t *>(calloc(5 * (size_t)max_forwards, sizeof(cudaEvent_t)));
+    if (!c->prof_ev) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 5 * max_forwards; ++i)
+        if (cudaEventCreate(&c->prof_ev[i]) != cudaSuccess) {
+            c->prof_max = i / 5 + 1;
+            profile_release(c);
+            return MOE_ERR_CUDA;
+        }
+    c->prof_max = max_forwards;
+    c->prof_n = 0;
+    return MOE_OK;
+}
+
+int moe_profile_end(moe_ctx *c, float *stage_ms, int *n_forwards) {
+    if (!c || !c->prof_ev) return MOE_ERR_INVALID_ARG;
+    float sum[4] = {0, 0, 0, 0};
+    int rc = MOE_OK;
+    for (int f = 0; f < c->prof_n && rc == MOE_OK; ++f) {
+        cudaEvent_t *ev = c->prof_ev + 5 * f;
+        if (cudaEventSynchronize(ev[4]) != cudaSuccess) rc = MOE_ERR_CUDA;
+        for (int st = 0; st < 4 && rc == MOE_OK; ++st) {
+            float ms = 0;
+            if (cudaEventElapsedTime(&ms, ev[st], ev[st + 1]) != cudaSuccess) rc = MOE_ERR_CUDA;
+            sum[st] += ms;
+        }
+    }
+    if (stage_ms) memcpy(stage_ms, sum, sizeof(sum));
+    if (n_forwards) *n_forwards = c->prof_n;
+    profile_release(c);
+    return rc;
+}
+
+int moe_device_status(moe_ctx *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    int err = 0;
+    if (cudaMemcpy(&err, c->ws + c->L.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (err && cudaMemset(c->ws + c->L.err, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (err & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    if (err & kErrBadExpert) return MOE_ERR_BAD_EXPERT;
+    return MOE_OK;
+}
+
+const char *moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or format";
+        case MOE_ERR_CUDA: return "CUDA call failed";
+        case MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+        case MOE_ERR_BAD_EXPERT: return "topk_idx holds an expert id outside [-1, E)";
+        case MOE_ERR_NOT_READY: return "weights not transformed yet";
+        default: return "unknown error";
+    }
+}
+
+void moe_destroy(moe_ctx *c) {
+    if (!c) return;
+    profile_release(c);
+    free(c);
+}
+
+}  // extern "C"

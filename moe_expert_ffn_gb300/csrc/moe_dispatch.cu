@@ -1,0 +1,146 @@
+// moe_dispatch.cu -- dispatch of routed (token, slot) pairs to experts.
+//
+// Per-expert counts, their exclusive prefix and the gather map that lists
+// each expert's pairs in (token, slot) order (MegaMoE SM90 Implementation
+// Design (Final), §9.2 "Dispatch Pull Path" and §21 Phase 2; PR357
+// Green-Context Split MegaMoE code review, §6.1 "Dispatch metadata").  On one
+// GPU the pages' cross-rank pull becomes this local map: the L1 GEMM then
+// reads token rows straight from x through it.
+//
+// One CTA of 1024 threads.  Each warp owns a contiguous segment of the pairs:
+// pass 1 builds a per-warp histogram, a scan over (expert, warp) gives every
+// warp its first slot inside each expert, pass 2 walks the segment in order
+// and ranks equal experts inside each 32-pair batch with __match_any_sync, so
+// the map is the stable order without any sort.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+// Exclusive block-wide scan of one value per thread (blockDim = 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += y;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+        if (lane == 31) *total = w;
+    }
+    __syncthreads();
+    const int before = warp ? warp_tot[warp - 1] : 0;
+    const int r = before + x - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dispatch_kernel(const int32_t *__restrict__ idx, int T, int k, int E, DispatchOut o) {
+    extern __shared__ int32_t sm[];
+    int32_t *hist = sm;                 // [kWarps][E]: count, then first slot of the warp
+    int32_t *off_s = sm + kWarps * E;   // [E+1]
+    __shared__ int warp_tot[kWarps];
+    __shared__ int tot_a, tot_b, bad;
+
+    const int P = T * k;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) hist[i] = 0;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+
+    const int seg = (P + kWarps - 1) / kWarps;
+    const int p0 = min(P, warp * seg), p1 = min(P, p0 + seg);
+
+    // pass 1: per-warp histogram
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const int e = __ldg(idx + p);
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[warp * E + e], 1);
+        else if (e != -1)
+            bad = 1;
+    }
+    __syncthreads();
+
+    // per expert: first slot of each warp inside the expert, and the count
+    int cnt = 0;
+    if (threadIdx.x < E) {
+        const int e = threadIdx.x;
+        for (int w = 0; w < kWarps; ++w) {
+            const int h = hist[w * E + e];
+            hist[w * E + e] = cnt;
+            cnt += h;
+        }
+    }
+    // E <= kThreads: one expert per thread for both prefix scans
+    const int nmb = (cnt + kBM - 1) / kBM;
+    const int off = block_exclusive_scan(cnt, warp_tot, &tot_a);
+    const int mbo = block_exclusive_scan(nmb, warp_tot, &tot_b);
+    if (threadIdx.x < E) {
+        off_s[threadIdx.x] = off;
+        o.count[threadIdx.x] = cnt;
+        o.offset[threadIdx.x] = off;
+        o.mb_prefix[threadIdx.x] = mbo;
+        if (o.stats) o.stats[threadIdx.x] += cnt;
+        for (int b = 0; b < nmb; ++b) o.mblk_expert[mbo + b] = threadIdx.x;
+    }
+    if (threadIdx.x == 0) {
+        off_s[E] = tot_a;
+        o.offset[E] = tot_a;
+        o.mb_prefix[E] = tot_b;
+        if (bad) atomicOr(o.err, kErrBadExpert);
+    }
+    __syncthreads();
+
+    // pass 2: stable positions, batch by batch in pair order
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = p0; base < p1; base += 32) {
+        const int p = base + lane;
+        const int e = (p < p1) ? __ldg(idx + p) : -1;
+        const bool ok = e >= 0 && e < E;
+        const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+        int rank = 0;
+        if (ok) {
+            rank = __popc(grp & lt_mask);
+            const int pos = off_s[e] + hist[warp * E + e] + rank;
+            o.gather[pos] = p;
+            o.pair_pool[p] = pos;
+        } else if (p < p1) {
+            o.pair_pool[p] = -1;
+        }
+        __syncwarp();
+        if (ok && rank == __popc(grp) - 1) hist[warp * E + e] += __popc(grp);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                     cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * (size_t)(kWarps * E + E + 1);
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(int32_t) * (kWarps * 1024 + 1025)));
+        configured = true;
+    }
+    dispatch_kernel<<<1, kThreads, smem, s>>>(topk_idx, T, k, E, o);
+}
+
+}  // namespace moe

@@ -1,0 +1,68 @@
+// moe_internal.h -- launch interface between the C ABI (moe_api.cu) and the
+// kernels (dispatch, grouped GEMMs, combine, weight transform).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBM = 128;   // pool rows (routed pairs) per M block
+constexpr int kBK = 128;   // K bytes per pipeline stage (one scale block)
+constexpr int kNMajorMinRows = 256;  // experts with at least this many pairs walk N-major
+
+// Dispatch result: where the pairs of each expert sit in the pool.
+struct DispatchOut {
+    int32_t *count;        // [E]
+    int32_t *offset;       // [E+1]  exclusive prefix of count
+    int32_t *mb_prefix;    // [E+1]  exclusive prefix of ceil(count/128)
+    int32_t *mblk_expert;  // [max M blocks]  expert of each M block
+    int32_t *gather;       // [T*k]  pool row -> pair id t*k+j (stable order)
+    int32_t *pair_pool;    // [T*k]  pair id -> pool row, -1 if inactive
+    int32_t *stats;        // [E] or null: += count
+    int *err;              // device error word
+};
+
+void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                     cudaStream_t s);
+
+// L1: x (gathered by pool row) . W1i^T, SwiGLU * w, per-64 FP8 requant.
+struct L1Params {
+    const int32_t *gather, *offset, *mb_prefix, *mblk_expert;
+    const float *x_sf;        // [T, H/128]
+    const float *topk_w;      // [T*k]
+    const float2 *w1_sf;      // [E, 2I/128, H/128] (gate scale, up scale) per interleaved block
+    uint8_t *l2_acts;         // [Pmax, I]
+    float *l2_sf;             // [I/64, Pmax]
+    int *err;
+    int H, I, E, k, Pmax;
+    float clamp;
+};
+void launch_l1(const CUtensorMap &tm_x, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
+               int num_sms, cudaStream_t s);
+
+// L2: l2_acts . W2^T with per-64 activation scales, BF16 out in pool order.
+struct L2Params {
+    const int32_t *offset, *mb_prefix, *mblk_expert;
+    const float *l2_sf;       // [I/64, Pmax]
+    const float *w2_sf;       // [E, H/128, I/128]
+    uint16_t *l2_out;         // [Pmax, H] bf16
+    int *err;
+    int H, I, E, Pmax;
+};
+void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
+               cudaStream_t s);
+
+// Combine: y[t] = bf16( sum_j bf16 l2_out[pair_pool[t*k+j]] ) in slot order.
+void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int k, int H,
+                    uint16_t *y, cudaStream_t s);
+
+// Weight transform (W1 gate/up interleave in groups of 8 rows, scale pairs).
+void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, float2 *w1i_sf,
+                         int E, int H, int I, cudaStream_t s);
+
+size_t l1_smem_bytes();
+size_t l2_smem_bytes();
+
+}  // namespace moe

@@ -166,37 +166,49 @@ def make_acts(wl: Workload, device="cpu"):
     return pack_fp8_rows_ue8m0(x, 32)
 
 
-def make_weights(wl: Workload, device="cpu"):
-    """Canonical (non-interleaved) W1 [E,2I,H] (gate rows [0,I), up rows [I,2I)) and W2 [E,H,I]."""
-    E, H, I = wl.E, wl.H, wl.I
-    g = _gen(device, wl.seed, 3)
+def make_expert_weights(wl: Workload, e: int, device="cpu"):
+    """Canonical weights of expert e alone (each expert has its own random stream)."""
+    H, I = wl.H, wl.I
+    g = _gen(device, wl.seed, 1000 + e)
+    a = torch.randn(2 * I, H, generator=g, device=device, dtype=torch.float32) * (1.0 / math.sqrt(H))
+    b = torch.randn(H, I, generator=g, device=device, dtype=torch.float32) * (1.0 / math.sqrt(I))
     if wl.wfmt == 0:
-        w1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
-        w1_sf = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
-        w2 = torch.empty(E, H, I, dtype=torch.uint8, device=device)
-        w2_sf = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
+        return pack_fp8_blocks(a) + pack_fp8_blocks(b)
+    return pack_e2m1_rows(a) + pack_e2m1_rows(b)
+
+
+def make_weights(wl: Workload, device="cpu", experts=None):
+    """Canonical (non-interleaved) W1 [E,2I,H] (gate rows [0,I), up rows [I,2I)) and W2 [E,H,I].
+
+    With ``experts`` (a list of expert ids) only those experts are generated,
+    stacked in that order."""
+    E, H, I = wl.E, wl.H, wl.I
+    ids = list(range(E)) if experts is None else [int(e) for e in experts]
+    n = len(ids)
+    if wl.wfmt == 0:
+        w1 = torch.empty(n, 2 * I, H, dtype=torch.uint8, device=device)
+        w1_sf = torch.empty(n, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
+        w2 = torch.empty(n, H, I, dtype=torch.uint8, device=device)
+        w2_sf = torch.empty(n, H // 128, I // 128, dtype=torch.float32, device=device)
     else:
-        w1 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        w1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=device)
-        w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
-        w2_sf = torch.empty(E, H, I // 32, dtype=torch.uint8, device=device)
-    for e in range(E):
-        a = torch.randn(2 * I, H, generator=g, device=device, dtype=torch.float32) * (1.0 / math.sqrt(H))
-        b = torch.randn(H, I, generator=g, device=device, dtype=torch.float32) * (1.0 / math.sqrt(I))
-        if wl.wfmt == 0:
-            w1[e], w1_sf[e] = pack_fp8_blocks(a)
-            w2[e], w2_sf[e] = pack_fp8_blocks(b)
-        else:
-            w1[e], w1_sf[e] = pack_e2m1_rows(a)
-            w2[e], w2_sf[e] = pack_e2m1_rows(b)
-        del a, b
+        w1 = torch.empty(n, 2 * I, H // 2, dtype=torch.uint8, device=device)
+        w1_sf = torch.empty(n, 2 * I, H // 32, dtype=torch.uint8, device=device)
+        w2 = torch.empty(n, H, I // 2, dtype=torch.uint8, device=device)
+        w2_sf = torch.empty(n, H, I // 32, dtype=torch.uint8, device=device)
+    for i, e in enumerate(ids):
+        w1[i], w1_sf[i], w2[i], w2_sf[i] = make_expert_weights(wl, e, device)
     return w1, w1_sf, w2, w2_sf
 
 
-def make_inputs(wl: Workload, device="cpu", weights: bool = True) -> dict:
+def make_inputs(wl: Workload, device="cpu", weights: bool = True, batch: int = 0) -> dict:
+    """All inputs of one forward.  ``batch`` selects an independent batch of
+    tokens and routing (same weights), e.g. one per data-parallel replica."""
+    if batch:
+        wl = dataclasses.replace(wl, seed=wl.seed + 7919 * batch)
     x, x_sf = make_acts(wl, device)
     idx, w = make_routing(wl, device)
     out = {"x": x, "x_sf": x_sf, "topk_idx": idx, "topk_weights": w}
     if weights:
-        out["w1"], out["w1_sf"], out["w2"], out["w2_sf"] = make_weights(wl, device)
+        base = dataclasses.replace(wl, seed=wl.seed - 7919 * batch) if batch else wl
+        out["w1"], out["w1_sf"], out["w2"], out["w2_sf"] = make_weights(base, device)
     return out

@@ -1,0 +1,179 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Dispatch maps bit-exact; L2 activations (FP8 codes and scales) stage by
+stage; y within the layer tolerance (normalised L2 <= 2e-3, max |err| <=
+3e-2 * rms(y_ref)) on small cases the oracle finishes in seconds (several
+tiles, ragged tails) and on sampled tokens of the full-size workloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from gpu_util import assert_y_close, bf16_bits_to_float, compare_y, new_layer, sub_inputs, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_ffn_gb300 import build
+    build.build()
+    import moe_expert_ffn_gb300 as mod
+    return mod
+
+
+def _run(m, wl, inp, **kw):
+    layer = new_layer(m, wl, DEV, **kw)
+    g = to_dev(inp, DEV)
+    layer.transform_weights(g["w1"], g["w1_sf"], g["w2"], g["w2_sf"])
+    y = layer.forward(g["x"], g["x_sf"], g["topk_idx"], g["topk_weights"])
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    return layer, g, y
+
+
+SMALL = [
+    moe_synth.WORKLOADS["tiny"],
+    moe_synth.custom(T=200, H=512, I=384, E=6, k=4, seed=31, name="ragged"),
+    moe_synth.custom(T=300, H=256, I=256, E=3, k=2, seed=32, name="nmajor"),
+    moe_synth.custom(T=50, H=384, I=128, E=40, k=3, seed=33, name="sparse"),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_dispatch_bit_exact(m, orc, wl):
+    inp = moe_synth.make_inputs(wl)
+    layer, g, _ = _run(m, wl, inp)
+    counts, offsets, gather = layer.get_dispatch(wl.T)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"], wl.E)
+    assert st == orc.OK
+    assert np.array_equal(counts.cpu().numpy(), oc)
+    assert np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_y_matches_oracle(m, orc, wl):
+    inp = moe_synth.make_inputs(wl)
+    _, _, y = _run(m, wl, inp)
+    ref = bf16_bits_to_float(orc.forward(inp))
+    rel, mx = assert_y_close(y, ref, wl.name)
+    print(f"{wl.name}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
+
+
+def test_l2_activations_stage_by_stage(m, orc):
+    wl = moe_synth.custom(T=64, H=512, I=256, E=4, k=2, seed=34)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, _ = _run(m, wl, inp)
+    _, offsets, gather = layer.get_dispatch(wl.T)
+    acts, sf, out = layer.get_intermediates(wl.T)
+    acts, sf, out, gather = acts.cpu().numpy(), sf.cpu().numpy(), out.cpu(), gather.cpu().numpy()
+    idx, w = inp["topk_idx"].numpy(), inp["topk_weights"].numpy()
+    code_mismatch = total = 0
+    for r in range(0, int(offsets[-1]), 7):
+        pair = int(gather[r])
+        t, j = divmod(pair, wl.k)
+        pr = orc.pair(inp, t, int(idx[t, j]), float(w[t, j]))
+        np.testing.assert_allclose(sf[:, r], pr["sf"], rtol=1e-5, atol=0)
+        code_mismatch += int((acts[r] != pr["q"]).sum())
+        total += wl.I
+        ob = bf16_bits_to_float(pr["ob"])
+        rel, _ = compare_y(out[r:r + 1], ob[None])
+        assert rel <= 1e-3, (r, rel)
+    assert code_mismatch <= 0.01 * total, (code_mismatch, total)
+
+
+def test_zero_tokens_and_inactive_slots(m, orc):
+    wl = moe_synth.custom(T=40, H=256, I=128, E=8, k=3, seed=35)
+    inp = moe_synth.make_inputs(wl)
+    inp["topk_idx"][::3, 1] = -1
+    inp["topk_idx"][5, :] = -1
+    layer, g, y = _run(m, wl, inp)
+    ref = bf16_bits_to_float(orc.forward(inp))
+    assert_y_close(y, ref, "inactive slots")
+    assert torch.all(y[5] == 0)
+    y0 = torch.empty(0, wl.H, dtype=torch.bfloat16, device=DEV)
+    layer.forward(g["x"][:0], g["x_sf"][:0], g["topk_idx"][:0], g["topk_weights"][:0], y=y0)
+    assert layer.device_status() == m.MOE_OK
+
+
+def test_repeat_calls_stats_and_token_order(m, orc):
+    wl = moe_synth.custom(T=96, H=256, I=256, E=8, k=2, seed=36)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, y1 = _run(m, wl, inp)
+    stats = torch.zeros(wl.E, dtype=torch.int32, device=DEV)
+    y2 = layer.forward(g["x"], g["x_sf"], g["topk_idx"], g["topk_weights"], stats=stats)
+    y3 = layer.forward(g["x"], g["x_sf"], g["topk_idx"], g["topk_weights"], stats=stats)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(y2, y3)
+    counts = torch.bincount(inp["topk_idx"].reshape(-1).long(), minlength=wl.E).int()
+    assert torch.equal(stats.cpu(), 2 * counts)
+    perm = torch.randperm(wl.T, generator=torch.Generator().manual_seed(3)).to(DEV)
+    yp = layer.forward(g["x"][perm].contiguous(), g["x_sf"][perm].contiguous(),
+                       g["topk_idx"][perm].contiguous(), g["topk_weights"][perm].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(yp, y1[perm])            # bit-exact: rows are computed independently
+
+
+def test_forward_host_matches_device(m):
+    wl = moe_synth.custom(T=33, H=256, I=128, E=4, k=2, seed=37)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, y = _run(m, wl, inp)
+    pinned = {n: inp[n].pin_memory() for n in ("x", "x_sf", "topk_idx", "topk_weights")}
+    yh = layer.forward_host(pinned["x"], pinned["x_sf"], pinned["topk_idx"], pinned["topk_weights"])
+    assert torch.equal(yh, y.cpu())
+
+
+def test_bad_expert_id_is_reported_and_skipped(m, orc):
+    wl = moe_synth.custom(T=16, H=256, I=128, E=4, k=2, seed=38)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, _ = _run(m, wl, inp)
+    bad = g["topk_idx"].clone()
+    bad[3, 1] = 77
+    layer.forward(g["x"], g["x_sf"], bad, g["topk_weights"])
+    assert layer.device_status() == m.MOE_ERR_BAD_EXPERT
+    assert layer.device_status() == m.MOE_OK     # cleared after reading
+    ref_inp = dict(inp)
+    ref_idx = inp["topk_idx"].clone()
+    ref_idx[3, 1] = -1
+    ref_inp["topk_idx"] = ref_idx
+    y = layer.forward(g["x"], g["x_sf"], bad, g["topk_weights"])
+    assert_y_close(y, bf16_bits_to_float(orc.forward(ref_inp)), "bad id skipped")
+    layer.device_status()
+
+
+def test_one_expert_takes_everything(m, orc):
+    wl = moe_synth.custom(T=700, H=256, I=128, E=4, k=1, seed=39)
+    inp = moe_synth.make_inputs(wl)
+    inp["topk_idx"][:] = 2
+    inp["topk_weights"][:] = 1.0
+    _, _, y = _run(m, wl, inp)
+    sel = np.arange(0, wl.T, 9, dtype=np.int32)
+    ref = bf16_bits_to_float(orc.forward(inp, tokens=sel))
+    assert_y_close(y[torch.from_numpy(sel).long().to(DEV)], ref, "one expert")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "wide"])
+def test_full_size_sampled_tokens(m, orc, name):
+    wl = moe_synth.WORKLOADS[name]
+    inp = moe_synth.make_inputs(wl, device=DEV)
+    layer = new_layer(m, wl, DEV)
+    layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    y = layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    counts, offsets, gather = layer.get_dispatch(wl.T)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
+    assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
+    rng = np.random.default_rng(7)
+    tokens = np.sort(rng.choice(wl.T, size=6, replace=False)).astype(np.int32)
+    sub = sub_inputs(inp, tokens)
+    ref = bf16_bits_to_float(orc.forward(sub))
+    rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, name)
+    print(f"{name}: sampled tokens {tokens.tolist()} rel L2 {rel:.2e} max/rms {mx:.2e}")
+    assert torch.isfinite(y.float()).all()
