@@ -145,6 +145,37 @@ MOE_API int moe_get_dispatch(moe_ctx *ctx, int32_t *counts, int32_t *offsets, in
 MOE_API int moe_get_intermediates(moe_ctx *ctx, void *l2_acts, float *l2_sf, void *l2_out,
                           void *stream);
 
+/* Largest problem moe_dispatch_noalloc accepts. */
+#define MOE_NOALLOC_MAX_PAIRS 65536   /* num_tokens * topk */
+#define MOE_NOALLOC_MAX_EXPERTS 1024
+
+/* The dispatch step alone, for callers that cannot allocate device memory
+ * and cannot hand this library a workspace: code that runs inside a host
+ * application or serving runtime which plans every device byte itself and
+ * offers its plugins no workspace hook, or a path where a cudaMalloc would
+ * stall the device or break the runtime's memory budget.  The pages have no
+ * counterpart of this entry point.
+ *
+ * Computes what moe_forward's dispatch computes (counts int32 [E], offsets
+ * int32 [E+1], gather int32 [T*k] with the first offsets[E] entries valid)
+ * from topk_idx int32 [T,k] (device), into caller device buffers, on
+ * `stream`.  It allocates nothing: the kernel's other scratch (pair -> row
+ * map, M-block tables, error word) lives in one fixed device array of about
+ * 270 KB inside this library, which every GPU that loads the library keeps
+ * until the process exits.
+ *  - Sizes: returns MOE_ERR_INVALID_ARG, launching nothing, when
+ *    num_tokens * topk > MOE_NOALLOC_MAX_PAIRS, num_experts >
+ *    MOE_NOALLOC_MAX_EXPERTS, topk outside [1, 32], or a pointer is NULL.
+ *  - The first call on a device looks up that array's device address (with
+ *    that device current); make this first call before any stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    the call clears what must start at zero.  Calls that overlap on the GPU
+ *    (two streams, or two host threads) race on it and must not be issued.
+ *  - Expert ids outside [-1, E) are skipped but not reported here. */
+MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tokens, int topk,
+                                 int num_experts, int32_t *counts, int32_t *offsets,
+                                 int32_t *gather, void *stream);
+
 /* Per-stage timing of the next `max_forwards` forwards: moe_profile_begin
  * creates CUDA events (no device memory) and every following moe_forward
  * records one event before its dispatch and one after each of its four

@@ -33,7 +33,8 @@ MOE_W_FP4_E2M1_UE8M0_32 = 1
 ABI_SYMBOLS = (
     "moe_workspace_bytes", "moe_weight_bytes", "moe_create", "moe_transform_weights",
     "moe_forward", "moe_forward_host", "moe_get_dispatch", "moe_get_intermediates",
-    "moe_profile_begin", "moe_profile_end", "moe_device_status", "moe_strerror", "moe_destroy",
+    "moe_dispatch_noalloc", "moe_profile_begin", "moe_profile_end", "moe_device_status",
+    "moe_strerror", "moe_destroy",
 )
 
 

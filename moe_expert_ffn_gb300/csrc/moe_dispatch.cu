@@ -12,6 +12,9 @@
 // warp its first slot inside each expert, pass 2 walks the segment in order
 // and ranks equal experts inside each 32-pair batch with __match_any_sync, so
 // the map is the stable order without any sort.
+#include <mutex>
+
+#include "moe.h"
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -144,3 +147,67 @@ void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const Dispatc
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_dispatch_noalloc: the same kernel with its scratch in a fixed device
+// array, for callers that cannot allocate (see include/moe.h).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNaPairs = MOE_NOALLOC_MAX_PAIRS;
+constexpr int kNaExperts = MOE_NOALLOC_MAX_EXPERTS;
+constexpr int kNaPairPool = 0;                                   // [kNaPairs]
+constexpr int kNaMbPrefix = kNaPairPool + kNaPairs;              // [kNaExperts + 1]
+constexpr int kNaMblk = kNaMbPrefix + kNaExperts + 64;           // [kNaPairs/128 + kNaExperts + 1]
+constexpr int kNaErr = kNaMblk + kNaPairs / moe::kBM + kNaExperts + 64;
+constexpr int kNaInts = kNaErr + 64;
+
+// Shared by every call on a device; holds the last call's tables.
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNaInts];
+
+constexpr int kNaMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_ptr[kNaMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (host code may
+// not use the symbol itself: on the host it names a stand-in, not the array).
+int noalloc_scratch(int32_t **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tokens, int topk,
+                                            int num_experts, int32_t *counts, int32_t *offsets,
+                                            int32_t *gather, void *stream) {
+    if (!topk_idx || !counts || !offsets || !gather) return MOE_ERR_INVALID_ARG;
+    if (num_tokens < 0 || topk < 1 || topk > 32 || num_experts < 1 || num_experts > kNaExperts)
+        return MOE_ERR_INVALID_ARG;
+    if ((long long)num_tokens * topk > kNaPairs) return MOE_ERR_INVALID_ARG;
+    int32_t *scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != MOE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    moe::DispatchOut o;
+    o.count = counts;
+    o.offset = offsets;
+    o.gather = gather;
+    o.pair_pool = scratch + kNaPairPool;
+    o.mb_prefix = scratch + kNaMbPrefix;
+    o.mblk_expert = scratch + kNaMblk;
+    o.stats = nullptr;
+    o.err = scratch + kNaErr;
+    // the error word is only ever OR-ed into: start it at zero
+    if (cudaMemsetAsync(o.err, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    moe::launch_dispatch(topk_idx, num_tokens, topk, num_experts, o, s);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,69 @@
+"""moe_dispatch_noalloc, the dispatch entry point for callers that cannot
+allocate device memory (a host runtime that plans every device byte itself
+and gives its plugins no workspace), against the dispatch that moe_forward
+runs, through the C ABI, on two calls in a row with different routings.
+
+Dispatch maps are integer results: the comparison is bit-exact.  Collected
+last on purpose (file name), so a run that stops at its first failure has
+already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_fn(m):
+    raw = ctypes.CDLL(m.LIB_PATH)
+    fn = raw.moe_dispatch_noalloc
+    vp = ctypes.c_void_p
+    fn.restype = ctypes.c_int
+    fn.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
+    return fn
+
+
+def test_noalloc_dispatch_matches_forward_dispatch():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_ffn_gb300 import build
+    build.build()
+    import moe_expert_ffn_gb300 as m
+    dev = torch.device("cuda:0")
+    fn = _noalloc_fn(m)
+    stream = torch.cuda.current_stream(dev)
+    wl = moe_synth.custom(T=700, H=256, I=128, E=48, k=6, seed=51)
+    layer = m.MoELayer(wl.T, wl.H, wl.I, wl.E, wl.k, device=dev)
+    w = moe_synth.make_weights(wl, device=dev)
+    layer.transform_weights(*w)
+    for call, (seed, T) in enumerate(((52, 700), (53, 333))):
+        inp = moe_synth.make_inputs(moe_synth.custom(T=T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, seed=seed),
+                                    device=dev, weights=False)
+        if call == 1:
+            inp["topk_idx"][::5, 2] = -1            # some inactive slots on the second call
+        layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
+        ref_c, ref_o, ref_g = layer.get_dispatch(T)
+        counts = torch.full((wl.E,), -7, dtype=torch.int32, device=dev)
+        offsets = torch.full((wl.E + 1,), -7, dtype=torch.int32, device=dev)
+        gather = torch.full((T * wl.k,), -7, dtype=torch.int32, device=dev)
+        rc = fn(ctypes.c_void_p(inp["topk_idx"].data_ptr()), T, wl.k, wl.E,
+                ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(offsets.data_ptr()),
+                ctypes.c_void_p(gather.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        assert rc == m.MOE_OK, m.strerror(rc)
+        torch.cuda.synchronize(dev)
+        P = int(ref_o[-1])
+        assert torch.equal(counts, ref_c), f"call {call}: counts"
+        assert torch.equal(offsets, ref_o), f"call {call}: offsets"
+        assert torch.equal(gather[:P], ref_g[:P]), f"call {call}: gather"
+        assert P == int((inp["topk_idx"] >= 0).sum())
+    assert layer.device_status() == m.MOE_OK
+    # sizes beyond the fixed scratch are refused before anything is launched
+    big = int(65536 // wl.k) + 1
+    rc = fn(ctypes.c_void_p(inp["topk_idx"].data_ptr()), big, wl.k, wl.E,
+            ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(offsets.data_ptr()),
+            ctypes.c_void_p(gather.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    assert rc == m.MOE_ERR_INVALID_ARG
