@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller profiling cases; not a bench line)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T")
     return ap.parse_args()
 
 
@@ -389,6 +392,11 @@ def main():
     if args.workload not in moe_synth.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}")
     wl = moe_synth.WORKLOADS[args.workload]
+    if args.experts or args.tokens:
+        import dataclasses
+        E = args.experts or wl.E
+        T = args.tokens or wl.T
+        wl = dataclasses.replace(wl, E=E, T=T, name=f"{wl.name}_T{T}_E{E}")
     if args.impl == "reference":
         out = run_reference(args, wl, rank, world)
     else:

@@ -175,6 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tok[i] = r < t.rows ? __ldg(p.gather + t.row0 + r) / p.k : 0;
             }
             const int wrow = t.e * 2 * p.I + t.nb * kL1BN;
+            // only the gather4 requests that carry valid rows: the other smem
+            // rows keep stale bytes, which reach only masked accumulator rows
+            const int n_g4 = (t.rows + 3) >> 2;
+            const uint32_t tx = (uint32_t)n_g4 * 4 * kBK + kL1BBytes;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kL1Stages;
                 const uint32_t ph = (it / kL1Stages) & 1;
@@ -183,10 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t full = smem_u32(&ctrl->full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(full, kL1StageBytes);
+                if (lane == 0) mbar_arrive_expect_tx(full, tx);
                 __syncwarp();
                 const uint32_t a_dst = base + s * kL1StageBytes + lane * 512;
-                tma_gather4(a_dst, &tm_x, kb * kBK, tok[0], tok[1], tok[2], tok[3], full, pol_x);
+                if ((int)lane < n_g4)
+                    tma_gather4(a_dst, &tm_x, kb * kBK, tok[0], tok[1], tok[2], tok[3], full, pol_x);
                 if (lane == 0)
                     tma_load_2d(base + s * kL1StageBytes + kL1ABytes, &tm_w1, kb * kBK, wrow, full,
                                 pol_w);
@@ -252,11 +257,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
+            // scale factors prefetched two K blocks ahead (global-load latency
+            // would otherwise sit on the critical path of every block)
+            float sa1 = valid ? __ldg(sfa) : 0.0f;
+            float2 sb1 = __ldg(sfb);
+            float sa2 = (valid && KB > 1) ? __ldg(sfa + 1) : 0.0f;
+            float2 sb2 = KB > 1 ? __ldg(sfb + 1) : make_float2(0.0f, 0.0f);
             for (int kb = 0; kb < KB; ++kb, ++kt) {
                 const int b = kt & 1;
                 const uint32_t tph = (kt >> 1) & 1;
-                const float sa = valid ? __ldg(sfa + kb) : 0.0f;
-                const float2 sb = __ldg(sfb + kb);
+                const float sa = sa1;
+                const float2 sb = sb1;
+                sa1 = sa2;
+                sb1 = sb2;
+                if (kb + 2 < KB) {
+                    sa2 = valid ? __ldg(sfa + kb + 2) : 0.0f;
+                    sb2 = __ldg(sfb + kb + 2);
+                }
                 const float sg = sa * sb.x, su = sa * sb.y;
                 if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
                     ok = false;
@@ -429,13 +446,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
 
+            // scales prefetched two K blocks ahead
+            const float *sfa = p.l2_sf + row;
+            const size_t ps = (size_t)p.Pmax;
+            float2 a1 = valid ? make_float2(__ldg(sfa), __ldg(sfa + ps)) : make_float2(0.0f, 0.0f);
+            float b1 = __ldg(sfb);
+            float2 a2 = (valid && KB > 1) ? make_float2(__ldg(sfa + 2 * ps), __ldg(sfa + 3 * ps))
+                                          : make_float2(0.0f, 0.0f);
+            float b2 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
             for (int kb = 0; kb < KB; ++kb, ++kt) {
                 const int b = kt & 1;
                 const uint32_t tph = (kt >> 1) & 1;
-                const float sb = __ldg(sfb + kb);
-                const float sa0 = valid ? __ldg(p.l2_sf + (size_t)(2 * kb) * p.Pmax + row) : 0.0f;
-                const float sa1 = valid ? __ldg(p.l2_sf + (size_t)(2 * kb + 1) * p.Pmax + row) : 0.0f;
-                const float s0 = sa0 * sb, s1 = sa1 * sb;
+                const float2 sa = a1;
+                const float sb = b1;
+                a1 = a2;
+                b1 = b2;
+                if (kb + 2 < KB) {
+                    if (valid)
+                        a2 = make_float2(__ldg(sfa + (size_t)(2 * kb + 4) * ps),
+                                         __ldg(sfa + (size_t)(2 * kb + 5) * ps));
+                    b2 = __ldg(sfb + kb + 2);
+                }
+                const float s0 = sa.x * sb, s1 = sa.y * sb;
                 if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
                     ok = false;
                     break;
