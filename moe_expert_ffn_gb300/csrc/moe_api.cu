@@ -20,7 +20,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
     // workspace
     size_t err, count, offset, mb_prefix, mblk_expert, gather, pair_pool;
-    size_t l2_acts, l2_sf, l2_out;
+    size_t pool, l2_acts, l2_sf, l2_out;
     size_t st_x, st_xsf, st_idx, st_w, st_y;
     size_t ws_total;
     // weights
@@ -62,6 +62,7 @@ Layout make_layout(const moe_config *c) {
     L.mblk_expert = take(4 * MBmax, 256);
     L.gather = take(4 * Pm, 256);
     L.pair_pool = take(4 * Pm, 256);
+    L.pool = take(Pm * H, kAlign);
     L.l2_acts = take(Pm * I, kAlign);
     L.l2_sf = take(4 * (I / 64) * Pm, kAlign);
     L.l2_out = take(2 * Pm * H, kAlign);
@@ -127,7 +128,8 @@ struct moe_ctx {
     uint8_t *wt;
     bool weights_ready;
     int last_T;
-    CUtensorMap tm_w1, tm_w2, tm_l2a;
+    CUtensorMap tm_w1, tm_w2, tm_l2a, tm_pool;
+    int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
     int prof_max, prof_n;
 
@@ -169,10 +171,17 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     const uint64_t Pm = (uint64_t)g.max_tokens * g.topk;
     bool ok = make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
               make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128) &&
-              make_map(&c->tm_l2a, c->ws + c->L.l2_acts, I, Pm, I, 128, 128);
+              make_map(&c->tm_l2a, c->ws + c->L.l2_acts, I, Pm, I, 128, 128) &&
+              make_map(&c->tm_pool, c->ws + c->L.pool, H, Pm, H, 128, 128);
     if (!ok) {
         free(c);
         return MOE_ERR_CUDA;
+    }
+    // A operand of the L1 GEMM: MOE_L1_A=gather|pool overrides the automatic choice
+    c->l1_a_mode = 0;
+    if (const char *m = getenv("MOE_L1_A")) {
+        if (!strcmp(m, "gather")) c->l1_a_mode = 1;
+        if (!strcmp(m, "pool")) c->l1_a_mode = 2;
     }
     // zero the error word
     if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * 4) != cudaSuccess) {
@@ -234,8 +243,16 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     launch_dispatch(topk_idx, T, k, E, o, s);
     if (ev) cudaEventRecord(ev[1], s);
 
+    // A operand: gather token rows in the L1 producer (tile::gather4) when the
+    // M blocks are sparse, else copy them once into the pool
+    const bool gather_a = c->l1_a_mode ? c->l1_a_mode == 1 : (long long)T * k <= 4LL * E;
     CUtensorMap tm_x;
-    if (!make_map(&tm_x, x, (uint64_t)H, (uint64_t)T, (uint64_t)H, 128, 1)) return MOE_ERR_CUDA;
+    if (gather_a) {
+        if (!make_map(&tm_x, x, (uint64_t)H, (uint64_t)T, (uint64_t)H, 128, 1)) return MOE_ERR_CUDA;
+    } else {
+        launch_pool_gather(static_cast<const uint8_t *>(x), o.gather, o.offset + E, k, H, T * k,
+                           c->w<uint8_t>(L.pool), s);
+    }
 
     L1Params p1;
     p1.gather = o.gather;
@@ -254,7 +271,7 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     p1.k = k;
     p1.Pmax = Pm;
     p1.clamp = g.act_clamp;
-    launch_l1(tm_x, c->tm_w1, p1, g.fast_math, c->num_sms, s);
+    launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
     if (ev) cudaEventRecord(ev[2], s);
 
     L2Params p2;

@@ -115,6 +115,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -201,6 +206,18 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
 }
 
 // ---- small numerics ----------------------------------------------------------
+// {a0, a1} += {v0, v1} * s  as one packed FP32x2 FMA (round to nearest).
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float v0, float v1, float s) {
+    asm("{\n\t.reg .b64 acc, val, scl;\n\t"
+        "mov.b64 acc, {%0, %1};\n\t"
+        "mov.b64 val, {%2, %3};\n\t"
+        "mov.b64 scl, {%4, %4};\n\t"
+        "fma.rn.f32x2 acc, val, scl, acc;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(v0), "f"(v1), "f"(s));
+}
+
 // Two floats -> two E4M3 codes (round to nearest even, saturating), lo in bits 0..7.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t r;

@@ -60,7 +60,7 @@ constexpr size_t kCtrlBytes = 1024;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
 
 struct Tile {
-    int e, row0, rows, nb;
+    int e, row0, rows, nb, nmb;   // nmb: M blocks of expert e
 };
 
 // Tile `tile` of a grouped GEMM with NB column blocks: experts in ascending
@@ -90,6 +90,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__r
     t.row0 = off + mb * kBM;
     t.rows = min(kBM, cnt - mb * kBM);
     t.nb = nb;
+    t.nmb = nmb;
     return t;
 }
 
@@ -138,9 +139,12 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem, int warp) {
 // ============================================================================
 // L1: gate/up GEMM + SwiGLU * w + per-64 FP8 requantisation
 // ============================================================================
-template <bool kFast>
+// kGatherA: A rows gathered from x by token with tile::gather4 (tm_a = x,
+// boxes one row high); otherwise A is the pool of gathered rows written by
+// the dispatch step (tm_a = pool, 128-row boxes).
+template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
-    l1_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w1,
+    l1_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w1,
               const L1Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = __ldg(p.mb_prefix + p.E) * NB;
 
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_w1);
     }
     const uint32_t tmem = gemm_setup(ctrl, kL1Stages, warp);
@@ -162,23 +166,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        const uint64_t pol_w = policy_evict_first();
+        // weights of an expert with one M block are read once (evict first);
+        // with several M blocks the tile is shared by neighbouring CTAs
+        const uint64_t pol_once = policy_evict_first();
+        const uint64_t pol_shared = policy_evict_normal();
         const uint64_t pol_x = policy_evict_last();
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
-            int tok[4];
+            const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
+            int tok[4] = {0, 0, 0, 0};
+            if (kGatherA) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = (int)lane * 4 + i;
-                tok[i] = r < t.rows ? __ldg(p.gather + t.row0 + r) / p.k : 0;
+                for (int i = 0; i < 4; ++i) {
+                    const int r = (int)lane * 4 + i;
+                    tok[i] = r < t.rows ? __ldg(p.gather + t.row0 + r) / p.k : 0;
+                }
             }
             const int wrow = t.e * 2 * p.I + t.nb * kL1BN;
-            // only the gather4 requests that carry valid rows: the other smem
+            // gather4: only the requests that carry valid rows; the other smem
             // rows keep stale bytes, which reach only masked accumulator rows
             const int n_g4 = (t.rows + 3) >> 2;
-            const uint32_t tx = (uint32_t)n_g4 * 4 * kBK + kL1BBytes;
+            const uint32_t tx = kGatherA ? (uint32_t)n_g4 * 4 * kBK + kL1BBytes : kL1StageBytes;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kL1Stages;
                 const uint32_t ph = (it / kL1Stages) & 1;
@@ -189,9 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full = smem_u32(&ctrl->full[s]);
                 if (lane == 0) mbar_arrive_expect_tx(full, tx);
                 __syncwarp();
-                const uint32_t a_dst = base + s * kL1StageBytes + lane * 512;
-                if ((int)lane < n_g4)
-                    tma_gather4(a_dst, &tm_x, kb * kBK, tok[0], tok[1], tok[2], tok[3], full, pol_x);
+                if (kGatherA) {
+                    if ((int)lane < n_g4)
+                        tma_gather4(base + s * kL1StageBytes + lane * 512, &tm_a, kb * kBK, tok[0],
+                                    tok[1], tok[2], tok[3], full, pol_x);
+                } else if (lane == 0) {
+                    tma_load_2d(base + s * kL1StageBytes, &tm_a, kb * kBK, t.row0, full, pol_x);
+                }
                 if (lane == 0)
                     tma_load_2d(base + s * kL1StageBytes + kL1ABytes, &tm_w1, kb * kBK, wrow, full,
                                 pol_w);
@@ -289,11 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tcol + c * 32 + 32, v1);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = fmaf(v0[i], (i & 8) ? su : sg, acc[c * 32 + i]);
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v0[i], v0[i + 1],
+                                  (i & 8) ? su : sg);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + 32 + i] = fmaf(v1[i], (i & 8) ? su : sg, acc[c * 32 + 32 + i]);
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[c * 32 + 32 + i], acc[c * 32 + 33 + i], v1[i], v1[i + 1],
+                                  (i & 8) ? su : sg);
                     }
                 }
                 tc_fence_before();
@@ -368,12 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_once = policy_evict_first();
+            const uint64_t pol_shared = policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+                const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
                 const int wrow = t.e * p.H + t.nb * kL2BN;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kL2Stages;
@@ -482,9 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(c0 + 128 + c * 32, v1);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v0[i], s0, acc[c * 32 + i]);
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v0[i], v0[i + 1], s0);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v1[i], s1, acc[c * 32 + i]);
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v1[i], v1[i + 1], s1);
                     }
                 }
                 tc_fence_before();
@@ -507,20 +527,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t l1_smem_bytes() { return 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes; }
 size_t l2_smem_bytes() { return 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes; }
 
-void launch_l1(const CUtensorMap &tm_x, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
-               int num_sms, cudaStream_t s) {
+template <bool kFast, bool kGatherA>
+static void launch_l1_t(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
+                        int num_sms, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
-        cudaFuncSetAttribute(l1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)l1_smem_bytes());
-        cudaFuncSetAttribute(l1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(l1_kernel<kFast, kGatherA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)l1_smem_bytes());
         configured = true;
     }
-    if (fast_math)
-        l1_kernel<true><<<num_sms, kThreads, l1_smem_bytes(), s>>>(tm_x, tm_w1, p);
-    else
-        l1_kernel<false><<<num_sms, kThreads, l1_smem_bytes(), s>>>(tm_x, tm_w1, p);
+    l1_kernel<kFast, kGatherA><<<num_sms, kThreads, l1_smem_bytes(), s>>>(tm_a, tm_w1, p);
+}
+
+void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
+               bool gather_a, int num_sms, cudaStream_t s) {
+    if (fast_math) {
+        if (gather_a) launch_l1_t<true, true>(tm_a, tm_w1, p, num_sms, s);
+        else launch_l1_t<true, false>(tm_a, tm_w1, p, num_sms, s);
+    } else {
+        if (gather_a) launch_l1_t<false, true>(tm_a, tm_w1, p, num_sms, s);
+        else launch_l1_t<false, false>(tm_a, tm_w1, p, num_sms, s);
+    }
 }
 
 void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,

@@ -39,8 +39,15 @@ struct L1Params {
     int H, I, E, k, Pmax;
     float clamp;
 };
-void launch_l1(const CUtensorMap &tm_x, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
-               int num_sms, cudaStream_t s);
+// gather_a: tm_a maps x [T, H] with one-row boxes (rows gathered in the
+// kernel); otherwise tm_a maps the pool [Pmax, H] with 128-row boxes.
+void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
+               bool gather_a, int num_sms, cudaStream_t s);
+
+// Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
+// first offset[E] rows (rows_bound = T*k is the host-side upper bound).
+void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *offset_E, int k,
+                        int H, int rows_bound, uint8_t *pool, cudaStream_t s);
 
 // L2: l2_acts . W2^T with per-64 activation scales, BF16 out in pool order.
 struct L2Params {
