@@ -181,6 +181,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -206,18 +220,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
 }
 
 // ---- small numerics ----------------------------------------------------------
-// {a0, a1} += {v0, v1} * s  as one packed FP32x2 FMA (round to nearest).
-__device__ __forceinline__ void ffma2(float &a0, float &a1, float v0, float v1, float s) {
-    asm("{\n\t.reg .b64 acc, val, scl;\n\t"
-        "mov.b64 acc, {%0, %1};\n\t"
-        "mov.b64 val, {%2, %3};\n\t"
-        "mov.b64 scl, {%4, %4};\n\t"
-        "fma.rn.f32x2 acc, val, scl, acc;\n\t"
-        "mov.b64 {%0, %1}, acc;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(v0), "f"(v1), "f"(s));
-}
-
 // Two floats -> two E4M3 codes (round to nearest even, saturating), lo in bits 0..7.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t r;

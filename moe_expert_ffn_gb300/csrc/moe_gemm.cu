@@ -9,55 +9,70 @@
 // rounded to BF16.
 //
 // Both kernels are persistent (one CTA per SM) and walk a tile list derived
-// on the device from the dispatch counts (design §12: experts in order, N-major
-// inside experts with many rows).  Warp roles, 10 warps:
-//   warp 0      TMA producer (token rows gathered from x with tile::gather4 in
-//               L1; plain 2-D tiles elsewhere), multi-stage smem ring;
-//   warp 1      TMEM allocation, then MMA issuer: one thread issues
-//               tcgen05.mma kind::f8f6f4 into TMEM; every 128-K block (L1) or
-//               64-K half (L2) gets its own accumulator so the float block
-//               scales can be applied exactly;
-//   warps 2-9   epilogue (warp w reads TMEM lanes 32*(w%4)..+31): tcgen05.ld each finished block accumulator, FMA it
-//               into FP32 registers with its scale product (the pages'
-//               "promotion"), then SwiGLU/quantise (L1) or BF16 (L2) and store.
-// TMEM holds two accumulator buffers so the MMA of block k+1 overlaps the
-// promotion of block k.
+// on the device from the dispatch counts (design §12: experts in order,
+// N-major inside experts with many rows).  Warp roles, 10 warps:
+//   warp 0     TMA producer: multi-stage smem ring (A: 128 rows x 128 K bytes,
+//              token rows gathered from x with tile::gather4 or one 2-D box of
+//              the pool; B: weight rows x 128 K bytes);
+//   warp 1     TMEM allocation, then MMA issuer: one thread issues
+//              tcgen05.mma kind::f8f6f4 (M=128, K=32) into a ring of FP32
+//              accumulators in TMEM.  Every scale block gets its own
+//              accumulator (L1: one per 128-K block; L2: one per 64-K half, the
+//              pages' "dual-half" scaling) so the float scales can be applied
+//              exactly;
+//   warps 2-9  epilogue, two per TMEM lane quadrant (warp w reads lanes
+//              32*(w%4)..+31: one pool row per thread, half of the tile's
+//              columns per warp): tcgen05.ld each finished accumulator,
+//              release it, and FMA it into FP32 registers with its scale
+//              product (the pages' "promotion"); after the last block,
+//              SwiGLU/requantise (L1) or BF16 (L2) and store.
+// L1: 128 x 256 tiles (128 gate/up pairs = two 64-column output groups), two
+// 256-column accumulators.  L2: 128 x 128 tiles, a ring of four 128-column
+// accumulators (one per 64-K half).  Register budget: 168 per thread; the
+// epilogue keeps 128 (L1) or 64 (L2) accumulators and loads TMEM in small
+// pieces so nothing spills.
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;      // 10 warps: 200 registers per thread
+constexpr int kThreads = 320;
 constexpr int kNumEpiWarps = 8;
-constexpr int kEpiWarp0 = 2;       // warps 2..9 run the epilogue
+constexpr int kEpiWarp0 = 2;                 // warps 2..9 run the epilogue
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxStages = 6;
+constexpr int kMaxTBufs = 4;
 
-constexpr int kL1BN = 256;            // interleaved W1 rows per tile (128 gate/up pairs)
+// L1: 128 x 256 tiles, two 256-column accumulators, 4 stages of 48 KB
+constexpr int kL1BN = 256;
+constexpr int kL1TBufs = 2;
 constexpr int kL1Stages = 4;
 constexpr uint32_t kL1ABytes = kBM * kBK;
 constexpr uint32_t kL1BBytes = kL1BN * kBK;
 constexpr uint32_t kL1StageBytes = kL1ABytes + kL1BBytes;
-
-constexpr int kL2BN = 128;            // hidden columns per tile
+// L2: 128 x 128 tiles, four 128-column accumulators, 6 stages of 32 KB
+constexpr int kL2BN = 128;
+constexpr int kL2TBufs = 4;
 constexpr int kL2Stages = 6;
 constexpr uint32_t kL2ABytes = kBM * kBK;
 constexpr uint32_t kL2BBytes = kL2BN * kBK;
 constexpr uint32_t kL2StageBytes = kL2ABytes + kL2BBytes;
-
-constexpr int kMaxStages = 8;
+static_assert(kL1TBufs * kL1BN <= (int)kTmemCols && kL2TBufs * kL2BN <= (int)kTmemCols, "TMEM");
 
 struct alignas(8) Ctrl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tfull[kMaxTBufs];
+    uint64_t tempty[kMaxTBufs];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kCtrlBytes = 1024;
+constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
+constexpr size_t kL1SmemBytes = 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes;
+constexpr size_t kL2SmemBytes = 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes;
 
 struct Tile {
     int e, row0, rows, nb, nmb;   // nmb: M blocks of expert e
@@ -104,13 +119,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Common prologue: barriers, TMEM allocation.  Returns the TMEM base.
-__device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int stages, int warp) {
+__device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages, int tbufs) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
             mbar_init(smem_u32(&ctrl->empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < tbufs; ++b) {
             mbar_init(smem_u32(&ctrl->tfull[b]), 1);
             mbar_init(smem_u32(&ctrl->tempty[b]), kNumEpiWarps);
         }
@@ -133,6 +148,53 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem, int warp) {
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Release TMEM buffer b to the MMA warp (one arrival per epilogue warp).
+__device__ __forceinline__ void release_tbuf(Ctrl *ctrl, int b, uint32_t lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[b]));
+}
+
+// After a failed wait: let the producer's issued copies land before exit.
+__device__ __forceinline__ void drain_producer(Ctrl *ctrl, int it, int stages) {
+    for (int i = max(0, it - stages); i < it; ++i)
+        drain_wait(smem_u32(&ctrl->full[i % stages]), (i / stages) & 1);
+}
+
+// L1: promote this warp's 128 columns (TMEM columns tcol..tcol+127 of the
+// thread's lane) into acc[128] in 16-column pieces, and release the buffer
+// as soon as the last piece has landed.  Gate columns are 0-7 of every 16,
+// up columns 8-15: each piece has 8 of each.
+__device__ __forceinline__ void promote_l1(float (&acc)[128], uint32_t tcol, float s_gate,
+                                           float s_up, Ctrl *ctrl, int b, uint32_t lane) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float v[16];
+        tmem_ld16(tcol + 16 * c, v);
+        tmem_ld_wait();
+        if (c == 7) release_tbuf(ctrl, b, lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[16 * c + i] = fmaf(v[i], s_gate, acc[16 * c + i]);
+#pragma unroll
+        for (int i = 8; i < 16; ++i) acc[16 * c + i] = fmaf(v[i], s_up, acc[16 * c + i]);
+    }
+}
+
+// L2: promote this warp's 64 columns into acc[64], one scale for all.
+__device__ __forceinline__ void promote_l2(float (&acc)[64], uint32_t tcol, float sc, Ctrl *ctrl,
+                                           int b, uint32_t lane) {
+    float v0[32], v1[32];
+    tmem_ld32(tcol, v0);
+    tmem_ld32(tcol + 32, v1);
+    tmem_ld_wait();
+    release_tbuf(ctrl, b, lane);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        acc[i] = fmaf(v0[i], sc, acc[i]);
+        acc[32 + i] = fmaf(v1[i], sc, acc[32 + i]);
     }
 }
 
@@ -161,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_w1);
     }
-    const uint32_t tmem = gemm_setup(ctrl, kL1Stages, warp);
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs);
     volatile int *abort_flag = &ctrl->abort;
 
     if (warp == 0) {
@@ -211,21 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pol_w);
             }
         }
-        if (!ok) {  // let copies already issued land before the CTA exits
-            for (int i = max(0, it - kL1Stages); i < it; ++i)
-                drain_wait(smem_u32(&ctrl->full[i % kL1Stages]), (i / kL1Stages) & 1);
-        }
+        if (!ok) drain_producer(ctrl, it, kL1Stages);
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
-        int it = 0, kt = 0;
+        int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
+            for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kL1Stages;
                 const uint32_t ph = (it / kL1Stages) & 1;
-                const int b = kt & 1;
-                const uint32_t tph = (kt >> 1) & 1;
+                const int b = it % kL1TBufs;
+                const uint32_t tph = (it / kL1TBufs) & 1;
                 if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
                     !mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
                     ok = false;
@@ -251,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                  // TMEM lane quadrant this warp may access
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = q * 32 + (int)lane;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        const float clampv = p.clamp;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         int kt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -261,64 +319,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_on = q * 32 < t.rows;
             const int row = t.row0 + lrow;
             const int pair = valid ? __ldg(p.gather + row) : 0;
-            const int tok = pair / p.k;
-            const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
             const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
-            const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * p.I / 128) + jb) * KB;
-            const float *sfa = p.x_sf + (size_t)tok * KB;
+            const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
+            const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
 
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
-            // scale factors prefetched two K blocks ahead (global-load latency
-            // would otherwise sit on the critical path of every block)
-            float sa1 = valid ? __ldg(sfa) : 0.0f;
-            float2 sb1 = __ldg(sfb);
-            float sa2 = (valid && KB > 1) ? __ldg(sfa + 1) : 0.0f;
-            float2 sb2 = KB > 1 ? __ldg(sfb + 1) : make_float2(0.0f, 0.0f);
+            // scale factors prefetched one K block ahead
+            float sa_n = valid ? __ldg(sfa) : 0.0f;
+            float2 sb_n = __ldg(sfb);
             for (int kb = 0; kb < KB; ++kb, ++kt) {
-                const int b = kt & 1;
-                const uint32_t tph = (kt >> 1) & 1;
-                const float sa = sa1;
-                const float2 sb = sb1;
-                sa1 = sa2;
-                sb1 = sb2;
-                if (kb + 2 < KB) {
-                    sa2 = valid ? __ldg(sfa + kb + 2) : 0.0f;
-                    sb2 = __ldg(sfb + kb + 2);
+                const int b = kt % kL1TBufs;
+                const uint32_t tph = (kt / kL1TBufs) & 1;
+                const float sa = sa_n;
+                const float2 sb = sb_n;
+                if (kb + 1 < KB) {
+                    sa_n = valid ? __ldg(sfa + kb + 1) : 0.0f;
+                    sb_n = __ldg(sfb + kb + 1);
                 }
-                const float sg = sa * sb.x, su = sa * sb.y;
                 if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (warp_on) {
-                    const uint32_t tcol = t_lane + b * kL1BN + h * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; c += 2) {
-                        float v0[32], v1[32];
-                        tmem_ld32(tcol + c * 32, v0);
-                        tmem_ld32(tcol + c * 32 + 32, v1);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v0[i], v0[i + 1],
-                                  (i & 8) ? su : sg);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            ffma2(acc[c * 32 + 32 + i], acc[c * 32 + 33 + i], v1[i], v1[i + 1],
-                                  (i & 8) ? su : sg);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[b]));
+                if (warp_on)
+                    promote_l1(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
+                else
+                    release_tbuf(ctrl, b, lane);
             }
             if (!ok || !valid) continue;
 
             // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
+            const float wgt = __ldg(p.topk_w + pair);
+            const float clampv = p.clamp;
             float amax = 0.0f;
 #pragma unroll
             for (int o = 0; o < 64; ++o) {
@@ -348,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }
+            // this warp's 64 outputs are intermediate columns [64 jb, 64 jb + 64)
             uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.I + jb * 64);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
@@ -379,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_w2);
     }
-    const uint32_t tmem = gemm_setup(ctrl, kL2Stages, warp);
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs);
     volatile int *abort_flag = &ctrl->abort;
 
     if (warp == 0) {
@@ -407,50 +443,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pol_w);
                 }
             }
-            if (!ok) {
-                for (int i = max(0, it - kL2Stages); i < it; ++i)
-                    drain_wait(smem_u32(&ctrl->full[i % kL2Stages]), (i / kL2Stages) & 1);
-            }
+            if (!ok) drain_producer(ctrl, it, kL2Stages);
         }
         __syncwarp();
     } else if (warp == 1) {
+        // Each 128-K stage is two 64-K halves, each into its own accumulator.
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL2BN);
         int it = 0, kt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
+            for (int kb = 0; ok && kb < KB; ++kb, ++it) {
                 const int s = it % kL2Stages;
                 const uint32_t ph = (it / kL2Stages) & 1;
-                const int b = kt & 1;
-                const uint32_t tph = (kt >> 1) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
-                    !mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
+                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t ad = sw128_kmajor_desc(base + s * kL2StageBytes);
-                    const uint64_t bd = sw128_kmajor_desc(base + s * kL2StageBytes + kL2ABytes);
-                    const uint32_t d0 = tmem + b * 256;         // K half 0: columns [0,128)
-                    const uint32_t d1 = tmem + b * 256 + 128;   // K half 1: columns [128,256)
-                    umma_e4m3(d0, ad + 0, bd + 0, idesc, 0);
-                    umma_e4m3(d0, ad + 2, bd + 2, idesc, 1);
-                    umma_e4m3(d1, ad + 4, bd + 4, idesc, 0);
-                    umma_e4m3(d1, ad + 6, bd + 6, idesc, 1);
-                    umma_commit(smem_u32(&ctrl->empty[s]));
-                    umma_commit(smem_u32(&ctrl->tfull[b]));
+                const uint64_t ad = sw128_kmajor_desc(base + s * kL2StageBytes);
+                const uint64_t bd = sw128_kmajor_desc(base + s * kL2StageBytes + kL2ABytes);
+#pragma unroll
+                for (int half = 0; half < 2; ++half, ++kt) {
+                    const int b = kt % kL2TBufs;
+                    const uint32_t tph = (kt / kL2TBufs) & 1;
+                    if (!mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        umma_e4m3(tmem + b * kL2BN, ad + 4 * half, bd + 4 * half, idesc, 0);
+                        umma_e4m3(tmem + b * kL2BN, ad + 4 * half + 2, bd + 4 * half + 2, idesc, 1);
+                        umma_commit(smem_u32(&ctrl->tfull[b]));
+                    }
+                    __syncwarp();
                 }
+                if (ok && lane == 0) umma_commit(smem_u32(&ctrl->empty[s]));
                 __syncwarp();
             }
         }
-        if (!ok && it > 0)
-            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kL2Stages]), ((it - 1) / kL2Stages) & 1);
+        if (!ok && kt > 0)
+            drain_wait(smem_u32(&ctrl->tfull[(kt - 1) % kL2TBufs]), ((kt - 1) / kL2TBufs) & 1);
     } else {
         const int q = warp & 3;
         const int h = (warp - kEpiWarp0) >> 2;   // which 64 of the 128 tile columns
         const int lrow = q * 32 + (int)lane;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 64;
+        const size_t ps = (size_t)p.Pmax;
         int kt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -459,60 +497,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_on = q * 32 < t.rows;
             const int row = t.row0 + lrow;
             const float *sfb = p.w2_sf + ((size_t)t.e * NB + t.nb) * KB;
+            const float *sfa = p.l2_sf + row;   // 64-K half j of the K loop: sfa[j * Pmax]
+            const int NH = 2 * KB;
 
             float acc[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
 
-            // scales prefetched two K blocks ahead
-            const float *sfa = p.l2_sf + row;
-            const size_t ps = (size_t)p.Pmax;
-            float2 a1 = valid ? make_float2(__ldg(sfa), __ldg(sfa + ps)) : make_float2(0.0f, 0.0f);
-            float b1 = __ldg(sfb);
-            float2 a2 = (valid && KB > 1) ? make_float2(__ldg(sfa + 2 * ps), __ldg(sfa + 3 * ps))
-                                          : make_float2(0.0f, 0.0f);
-            float b2 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
-            for (int kb = 0; kb < KB; ++kb, ++kt) {
-                const int b = kt & 1;
-                const uint32_t tph = (kt >> 1) & 1;
-                const float2 sa = a1;
-                const float sb = b1;
-                a1 = a2;
-                b1 = b2;
-                if (kb + 2 < KB) {
-                    if (valid)
-                        a2 = make_float2(__ldg(sfa + (size_t)(2 * kb + 4) * ps),
-                                         __ldg(sfa + (size_t)(2 * kb + 5) * ps));
-                    b2 = __ldg(sfb + kb + 2);
-                }
-                const float s0 = sa.x * sb, s1 = sa.y * sb;
+            // scales prefetched two halves ahead (NH >= 2: I is a multiple of 128)
+            float sa1 = valid ? __ldg(sfa) : 0.0f;
+            float sa2 = valid ? __ldg(sfa + ps) : 0.0f;
+            float sb = __ldg(sfb);
+            for (int j = 0; j < NH; ++j, ++kt) {
+                const int b = kt % kL2TBufs;
+                const uint32_t tph = (kt / kL2TBufs) & 1;
+                const float sa = sa1;
+                sa1 = sa2;
+                if (j + 2 < NH && valid) sa2 = __ldg(sfa + (size_t)(j + 2) * ps);
+                if ((j & 1) == 0 && j > 0) sb = __ldg(sfb + (j >> 1));
+                const float sc = sa * sb;
                 if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (warp_on) {
-                    const uint32_t c0 = t_lane + b * 256 + h * 64;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float v0[32], v1[32];
-                        tmem_ld32(c0 + c * 32, v0);
-                        tmem_ld32(c0 + 128 + c * 32, v1);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v0[i], v0[i + 1], s0);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], v1[i], v1[i + 1], s1);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[b]));
+                if (warp_on)
+                    promote_l2(acc, t_lane + b * kL2BN, sc, ctrl, b, lane);
+                else
+                    release_tbuf(ctrl, b, lane);
             }
             if (!ok || !valid) continue;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + t.nb * kL2BN + h * 64);
+            uint4 *dst =
+                reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + t.nb * kL2BN + h * 64);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
                 dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]), bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
@@ -524,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t l1_smem_bytes() { return 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes; }
-size_t l2_smem_bytes() { return 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes; }
+size_t l1_smem_bytes() { return kL1SmemBytes; }
+size_t l2_smem_bytes() { return kL2SmemBytes; }
 
 template <bool kFast, bool kGatherA>
 static void launch_l1_t(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
@@ -533,10 +549,10 @@ static void launch_l1_t(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const
     static bool configured = false;
     if (!configured) {
         cudaFuncSetAttribute(l1_kernel<kFast, kGatherA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)l1_smem_bytes());
+                             (int)kL1SmemBytes);
         configured = true;
     }
-    l1_kernel<kFast, kGatherA><<<num_sms, kThreads, l1_smem_bytes(), s>>>(tm_a, tm_w1, p);
+    l1_kernel<kFast, kGatherA><<<num_sms, kThreads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
 }
 
 void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
@@ -554,11 +570,10 @@ void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params
                cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
-        cudaFuncSetAttribute(l2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)l2_smem_bytes());
+        cudaFuncSetAttribute(l2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
         configured = true;
     }
-    l2_kernel<<<num_sms, kThreads, l2_smem_bytes(), s>>>(tm_a, tm_w2, p);
+    l2_kernel<<<num_sms, kThreads, kL2SmemBytes, s>>>(tm_a, tm_w2, p);
 }
 
 }  // namespace moe
