@@ -498,33 +498,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = t.row0 + lrow;
             const float *sfb = p.w2_sf + ((size_t)t.e * NB + t.nb) * KB;
             const float *sfa = p.l2_sf + row;   // 64-K half j of the K loop: sfa[j * Pmax]
-            const int NH = 2 * KB;
 
             float acc[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
 
-            // scales prefetched two halves ahead (NH >= 2: I is a multiple of 128)
-            float sa1 = valid ? __ldg(sfa) : 0.0f;
-            float sa2 = valid ? __ldg(sfa + ps) : 0.0f;
-            float sb = __ldg(sfb);
-            for (int j = 0; j < NH; ++j, ++kt) {
-                const int b = kt % kL2TBufs;
-                const uint32_t tph = (kt / kL2TBufs) & 1;
-                const float sa = sa1;
-                sa1 = sa2;
-                if (j + 2 < NH && valid) sa2 = __ldg(sfa + (size_t)(j + 2) * ps);
-                if ((j & 1) == 0 && j > 0) sb = __ldg(sfb + (j >> 1));
-                const float sc = sa * sb;
-                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
+            // one 128-K block (two halves, two ring buffers) per iteration;
+            // scales prefetched one block ahead
+            float sa0_n = valid ? __ldg(sfa) : 0.0f;
+            float sa1_n = valid ? __ldg(sfa + ps) : 0.0f;
+            float sb_n = __ldg(sfb);
+            for (int kb = 0; kb < KB; ++kb, kt += 2) {
+                const float s0 = sa0_n * sb_n, s1 = sa1_n * sb_n;
+                if (kb + 1 < KB) {
+                    if (valid) {
+                        sa0_n = __ldg(sfa + (size_t)(2 * kb + 2) * ps);
+                        sa1_n = __ldg(sfa + (size_t)(2 * kb + 3) * ps);
+                    }
+                    sb_n = __ldg(sfb + kb + 1);
+                }
+                const int b0 = kt % kL2TBufs, b1 = (kt + 1) % kL2TBufs;
+                if (!mbar_wait(smem_u32(&ctrl->tfull[b0]), (kt / kL2TBufs) & 1, abort_flag, p.err) ||
+                    !mbar_wait(smem_u32(&ctrl->tfull[b1]), ((kt + 1) / kL2TBufs) & 1, abort_flag,
+                               p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (warp_on)
-                    promote_l2(acc, t_lane + b * kL2BN, sc, ctrl, b, lane);
-                else
-                    release_tbuf(ctrl, b, lane);
+                if (warp_on) {
+                    promote_l2(acc, t_lane + b0 * kL2BN, s0, ctrl, b0, lane);
+                    promote_l2(acc, t_lane + b1 * kL2BN, s1, ctrl, b1, lane);
+                } else {
+                    release_tbuf(ctrl, b0, lane);
+                    release_tbuf(ctrl, b1, lane);
+                }
             }
             if (!ok || !valid) continue;
             uint4 *dst =
