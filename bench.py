@@ -74,9 +74,14 @@ def work_model(wl, counts):
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     n_touch = int(sum(1 for c in counts if c > 0))
     P = int(sum(counts))
-    w1 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
-    w2 = H * I + (H // 128) * (I // 128) * 4
-    x = T * H + T * (H // 128) * 4
+    if wl.wfmt == 0:   # FP8 codes + f32 128x128 block scales
+        w1 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+        w2 = H * I + (H // 128) * (I // 128) * 4
+        x = T * H + T * (H // 128) * 4
+    else:              # packed E2M1 + UE8M0 per 32
+        w1 = 2 * I * H // 2 + 2 * I * H // 32
+        w2 = H * I // 2 + H * I // 32
+        x = T * H + T * (H // 32)
     routing = T * k * 8
     y = T * H * 2
     acts = P * I + P * (I // 64) * 4
@@ -217,10 +222,10 @@ def cpu_sample_inputs(wl, n_tokens, seed_offset=0):
             "w1": w1, "w1_sf": w1_sf, "w2": w2, "w2_sf": w2_sf}
 
 
-def time_oracle(inp):
+def time_oracle(inp, wfmt=0):
     import oracle
     t0 = time.perf_counter()
-    oracle.forward(inp, wfmt=0)
+    oracle.forward(inp, wfmt=wfmt)
     return time.perf_counter() - t0
 
 
@@ -234,8 +239,8 @@ def run_reference(args, wl, rank, world):
     n_tok = max(1, min(wl.T, threads))
     inp = cpu_sample_inputs(wl, n_tok)
     for _ in range(args.warmup):
-        time_oracle(inp)
-    times = [time_oracle(inp) for _ in range(args.steps)]
+        time_oracle(inp, wl.wfmt)
+    times = [time_oracle(inp, wl.wfmt) for _ in range(args.steps)]
     total = sum(times)
     value = n_tok * args.steps / total
     sample = (f"{n_tok} tokens x {wl.k} slots of the {wl.name} workload per step "
@@ -265,7 +270,7 @@ def run_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = moe_synth.make_inputs(wl, device=dev, batch=rank)
-    layer = m.MoELayer(wl.T, wl.H, wl.I, wl.E, wl.k, device=dev)
+    layer = m.MoELayer(wl.T, wl.H, wl.I, wl.E, wl.k, wfmt=wl.wfmt, device=dev)
     layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
     del inp["w1"], inp["w2"]
     y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
@@ -354,7 +359,8 @@ def run_ours(args, wl, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": world * wl.T / (ms / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate)" if wl.wfmt == 0 else "fp8_e4m3 x fp4_e2m1, ue8m0 block scales (fp32 accumulate)",
         "data": "synthetic (seeded, DeepSeek-V3-shaped, random-init weights)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "touched_experts": wm["n_touched"], "parallelism": f"dp{world} (independent replicas)",
@@ -376,7 +382,7 @@ def run_ours(args, wl, rank, world, local_rank):
         threads = oracle.num_threads()
         n_tok = max(1, min(wl.T, 2 * threads))
         cin = cpu_sample_inputs(wl, n_tok, seed_offset=1)
-        dt = time_oracle(cin)
+        dt = time_oracle(cin, wl.wfmt)
         out["cpu_baseline"] = {"value": n_tok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
                                "sample": f"{n_tok} tokens x {wl.k} slots of the {wl.name} workload "
                                          f"({dt:.1f} s wall on the host cores)"}

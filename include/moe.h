@@ -69,8 +69,8 @@ typedef struct moe_ctx moe_ctx;
  *   design §16.1 and §15.2).
  * MOE_W_FP4_E2M1_UE8M0_32: W1/W2 FP4 E2M1 (two codes per byte, low nibble =
  *   even k) with one UE8M0 scale per 1x32; activations FP8 E4M3 with one UE8M0
- *   scale per 1x32 (design §2.1, PR357 review §1).  Not yet run by this
- *   build: moe_create returns MOE_ERR_UNSUPPORTED. */
+ *   scale per 1x32; the L2 activations are requantised per 1x32 with UE8M0
+ *   scales 2^ceil(log2(amax/448)) (design §2.1, PR357 review §1, §6.1). */
 typedef enum { MOE_W_FP8_BLK128 = 0, MOE_W_FP4_E2M1_UE8M0_32 = 1 } moe_wfmt;
 
 typedef struct {
@@ -97,11 +97,13 @@ MOE_API int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, 
 
 /* Read the canonical weights and write the kernel layout into d_weights
  * (design §15: gate/up rows interleaved in groups of 8 along N).
- * Canonical layouts, all row-major (MOE_W_FP8_BLK128):
- *   w1    u8 (E4M3) [E, 2I, H]    rows [0, I) = gate, rows [I, 2I) = up
- *   w1_sf f32       [E, 2I/128, H/128]
- *   w2    u8 (E4M3) [E, H, I]
- *   w2_sf f32       [E, H/128, I/128]
+ * Canonical layouts, all row-major, rows [0, I) of w1 = gate, [I, 2I) = up.
+ * MOE_W_FP8_BLK128:
+ *   w1    u8 (E4M3) [E, 2I, H],   w1_sf f32 [E, 2I/128, H/128]
+ *   w2    u8 (E4M3) [E, H, I],    w2_sf f32 [E, H/128, I/128]
+ * MOE_W_FP4_E2M1_UE8M0_32 (32-byte aligned code arrays):
+ *   w1    u8 (2 x E2M1) [E, 2I, H/2],  w1_sf u8 (UE8M0) [E, 2I, H/32]
+ *   w2    u8 (2 x E2M1) [E, H, I/2],   w2_sf u8 (UE8M0) [E, H, I/32]
  * The inputs may be freed once the stream has passed this call. */
 MOE_API int moe_transform_weights(moe_ctx *ctx, const void *w1, const void *w1_sf,
                           const void *w2, const void *w2_sf, void *stream);
@@ -109,7 +111,7 @@ MOE_API int moe_transform_weights(moe_ctx *ctx, const void *w1, const void *w1_s
 /* One forward pass (design §3.3).
  *   num_tokens T, 0 <= T <= max_tokens (T = 0 returns at once)
  *   x             u8 (E4M3) [T, H] row-major, rows 16-byte aligned
- *   x_sf          f32 [T, H/128]
+ *   x_sf          f32 [T, H/128] (FP8 weights) or u8 UE8M0 [T, H/32] (FP4 weights)
  *   topk_idx      int32 [T, k]; -1 marks an inactive slot
  *   topk_weights  f32 [T, k]
  *   y             bf16 [T, H] (written)
@@ -139,10 +141,11 @@ MOE_API int moe_get_dispatch(moe_ctx *ctx, int32_t *counts, int32_t *offsets, in
 
 /* Copy intermediates of the last forward (T tokens; row r belongs to pair
  * gather[r], rows r >= offsets[E] unspecified), P = T*k:
- * l2_acts u8 (E4M3) [P, I], l2_sf f32 [I/64, P] (the L2 activation scales),
+ * l2_acts u8 (E4M3) [P, I], l2_sf = the L2 activation scales (f32 [I/64, P]
+ * with FP8 weights, u8 UE8M0 [P, I/32] with FP4 weights),
  * l2_out bf16 [P, H] (the rounded L2 outputs).  Any pointer may be NULL.
  * For stage-by-stage tests. */
-MOE_API int moe_get_intermediates(moe_ctx *ctx, void *l2_acts, float *l2_sf, void *l2_out,
+MOE_API int moe_get_intermediates(moe_ctx *ctx, void *l2_acts, void *l2_sf, void *l2_out,
                           void *stream);
 
 /* Largest problem moe_dispatch_noalloc accepts. */

@@ -162,12 +162,22 @@ class MoELayer:
             raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
         return t
 
+    @property
+    def fp4(self) -> bool:
+        return self.cfg.wfmt == MOE_W_FP4_E2M1_UE8M0_32
+
     def transform_weights(self, w1, w1_sf, w2, w2_sf, stream=None):
         E, H, I = self.E, self.H, self.I
-        self._cuda(w1, torch.uint8, (E, 2 * I, H), "w1")
-        self._cuda(w1_sf, torch.float32, (E, 2 * I // 128, H // 128), "w1_sf")
-        self._cuda(w2, torch.uint8, (E, H, I), "w2")
-        self._cuda(w2_sf, torch.float32, (E, H // 128, I // 128), "w2_sf")
+        if self.fp4:
+            self._cuda(w1, torch.uint8, (E, 2 * I, H // 2), "w1")
+            self._cuda(w1_sf, torch.uint8, (E, 2 * I, H // 32), "w1_sf")
+            self._cuda(w2, torch.uint8, (E, H, I // 2), "w2")
+            self._cuda(w2_sf, torch.uint8, (E, H, I // 32), "w2_sf")
+        else:
+            self._cuda(w1, torch.uint8, (E, 2 * I, H), "w1")
+            self._cuda(w1_sf, torch.float32, (E, 2 * I // 128, H // 128), "w1_sf")
+            self._cuda(w2, torch.uint8, (E, H, I), "w2")
+            self._cuda(w2_sf, torch.float32, (E, H // 128, I // 128), "w2_sf")
         _check(lib().moe_transform_weights(self._ctx, _ptr(w1), _ptr(w1_sf), _ptr(w2), _ptr(w2_sf),
                                            _stream(stream)), "moe_transform_weights")
 
@@ -175,7 +185,10 @@ class MoELayer:
         T = x.shape[0]
         H, k = self.H, self.k
         self._cuda(x, torch.uint8, (T, H), "x")
-        self._cuda(x_sf, torch.float32, (T, H // 128), "x_sf")
+        if self.fp4:
+            self._cuda(x_sf, torch.uint8, (T, H // 32), "x_sf")
+        else:
+            self._cuda(x_sf, torch.float32, (T, H // 128), "x_sf")
         self._cuda(topk_idx, torch.int32, (T, k), "topk_idx")
         self._cuda(topk_weights, torch.float32, (T, k), "topk_weights")
         if y is None:
@@ -211,7 +224,10 @@ class MoELayer:
     def get_intermediates(self, num_tokens, stream=None):
         P = max(num_tokens * self.k, 1)
         acts = torch.empty(P, self.I, dtype=torch.uint8, device=self.device)
-        sf = torch.empty(self.I // 64, P, dtype=torch.float32, device=self.device)
+        if self.fp4:
+            sf = torch.empty(P, self.I // 32, dtype=torch.uint8, device=self.device)
+        else:
+            sf = torch.empty(self.I // 64, P, dtype=torch.float32, device=self.device)
         out = torch.empty(P, self.H, dtype=torch.bfloat16, device=self.device)
         _check(lib().moe_get_intermediates(self._ctx, _ptr(acts), _ptr(sf), _ptr(out), _stream(stream)),
                "moe_get_intermediates")

@@ -74,10 +74,17 @@ Layout make_layout(const moe_config *c) {
     L.ws_total = align_up(o, kAlign);
 
     o = 0;
-    L.w1i = take(E * 2 * I * H, kAlign);
-    L.w1i_sf = take(8 * E * (2 * I / 128) * (H / 128), 256);
-    L.w2 = take(E * H * I, kAlign);
-    L.w2_sf = take(4 * E * (H / 128) * (I / 128), 256);
+    if (c->wfmt == MOE_W_FP8_BLK128) {
+        L.w1i = take(E * 2 * I * H, kAlign);
+        L.w1i_sf = take(8 * E * (2 * I / 128) * (H / 128), 256);
+        L.w2 = take(E * H * I, kAlign);
+        L.w2_sf = take(4 * E * (H / 128) * (I / 128), 256);
+    } else {   // packed E2M1 rows and per-32 UE8M0 scale rows
+        L.w1i = take(E * 2 * I * H / 2, kAlign);
+        L.w1i_sf = take(E * 2 * I * H / 32, 256);
+        L.w2 = take(E * H * I / 2, kAlign);
+        L.w2_sf = take(E * H * I / 32, 256);
+    }
     L.wt_total = align_up(o, kAlign);
     return L;
 }
@@ -100,22 +107,30 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D byte tensor [outer, inner] with row stride `stride` bytes, boxes of
-// box_inner x box_outer, 128-byte swizzle (box_inner must be 128).
+// 2-D tensor [outer, inner] with row stride `stride` bytes, boxes of
+// box_inner x box_outer elements, 128-byte swizzle.  Bytes (box_inner 128),
+// or packed 4-bit codes expanded to one byte each in shared memory
+// (16U4_ALIGN16B: inner counts codes, box_inner 128).
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_UINT8) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {stride};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+    return fn(m, dtype, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Bytes of the activation scales of T tokens.
+size_t x_sf_bytes(const moe_config &g, int T) {
+    return g.wfmt == MOE_W_FP8_BLK128 ? (size_t)T * (g.hidden / 128) * 4 : (size_t)T * (g.hidden / 32);
+}
 
 }  // namespace
 
@@ -154,7 +169,6 @@ size_t moe_weight_bytes(const moe_config *cfg) {
 int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_weights) {
     if (!out || !valid_cfg(cfg) || !d_workspace || !d_weights) return MOE_ERR_INVALID_ARG;
     if (!aligned(d_workspace, 256) || !aligned(d_weights, 256)) return MOE_ERR_INVALID_ARG;
-    if (cfg->wfmt != MOE_W_FP8_BLK128) return MOE_ERR_UNSUPPORTED;
     moe_ctx *c = static_cast<moe_ctx *>(calloc(1, sizeof(moe_ctx)));
     if (!c) return MOE_ERR_INVALID_ARG;
     c->cfg = *cfg;
@@ -169,8 +183,12 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     const moe_config &g = c->cfg;
     const uint64_t E = g.num_experts, H = g.hidden, I = g.inter;
     const uint64_t Pm = (uint64_t)g.max_tokens * g.topk;
-    bool ok = make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
-              make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128) &&
+    const bool fp4 = g.wfmt == MOE_W_FP4_E2M1_UE8M0_32;
+    const CUtensorMapDataType packed = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+    bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H / 2, 128, 128, packed) &&
+                         make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I / 2, 128, 128, packed)
+                   : make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
+                         make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128)) &&
               make_map(&c->tm_l2a, c->ws + c->L.l2_acts, I, Pm, I, 128, 128) &&
               make_map(&c->tm_pool, c->ws + c->L.pool, H, Pm, H, 128, 128);
     if (!ok) {
@@ -200,6 +218,21 @@ int moe_transform_weights(moe_ctx *c, const void *w1, const void *w1_sf, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const moe_config &g = c->cfg;
     const size_t E = g.num_experts, H = g.hidden, I = g.inter;
+    if (g.wfmt == MOE_W_FP4_E2M1_UE8M0_32) {
+        if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1_sf, 4) || !aligned(w2_sf, 4))
+            return MOE_ERR_INVALID_ARG;
+        launch_interleave_rows(static_cast<const uint8_t *>(w1), c->wt_at<uint8_t>(c->L.w1i), (int)E,
+                               (int)I, (int)(H / 2), s);
+        launch_interleave_rows(static_cast<const uint8_t *>(w1_sf), c->wt_at<uint8_t>(c->L.w1i_sf), (int)E,
+                               (int)I, (int)(H / 32), s);
+        if (cudaMemcpyAsync(c->wt + c->L.w2, w2, E * H * I / 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(c->wt + c->L.w2_sf, w2_sf, E * H * I / 32, cudaMemcpyDeviceToDevice, s) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+        c->weights_ready = true;
+        return MOE_OK;
+    }
     launch_transform_w1(static_cast<const uint8_t *>(w1), static_cast<const float *>(w1_sf),
                         c->wt_at<uint8_t>(c->L.w1i), c->wt_at<float2>(c->L.w1i_sf), (int)E, (int)H,
                         (int)I, s);
@@ -252,6 +285,38 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     } else {
         launch_pool_gather(static_cast<const uint8_t *>(x), o.gather, o.offset + E, k, H, T * k,
                            c->w<uint8_t>(L.pool), s);
+    }
+
+    if (g.wfmt == MOE_W_FP4_E2M1_UE8M0_32) {
+        Fp4Params f;
+        f.gather = o.gather;
+        f.offset = o.offset;
+        f.mb_prefix = o.mb_prefix;
+        f.mblk_expert = o.mblk_expert;
+        f.a_sf = static_cast<const uint8_t *>(x_sf);
+        f.b_sf = c->wt_at<uint8_t>(L.w1i_sf);
+        f.topk_w = topk_weights;
+        f.l2_acts = c->w<uint8_t>(L.l2_acts);
+        f.l2_sf = c->w<uint8_t>(L.l2_sf);
+        f.l2_out = c->w<uint16_t>(L.l2_out);
+        f.err = o.err;
+        f.H = H;
+        f.I = I;
+        f.E = E;
+        f.k = k;
+        f.Pmax = Pm;
+        f.clamp = g.act_clamp;
+        launch_fp4_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, f, g.fast_math, gather_a, c->num_sms, s);
+        if (ev) cudaEventRecord(ev[2], s);
+        f.a_sf = f.l2_sf;
+        f.b_sf = c->wt_at<uint8_t>(L.w2_sf);
+        launch_fp4_l2(c->tm_l2a, c->tm_w2, f, c->num_sms, s);
+        if (ev) cudaEventRecord(ev[3], s);
+        launch_combine(f.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);
+        if (ev) cudaEventRecord(ev[4], s);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+        c->last_T = T;
+        return MOE_OK;
     }
 
     L1Params p1;
@@ -309,7 +374,7 @@ int moe_forward_host(moe_ctx *c, int T, const void *h_x, const void *h_x_sf,
     const size_t H = g.hidden, k = g.topk;
     const Layout &L = c->L;
     if (cudaMemcpyAsync(c->ws + L.st_x, h_x, (size_t)T * H, cudaMemcpyHostToDevice, s) ||
-        cudaMemcpyAsync(c->ws + L.st_xsf, h_x_sf, (size_t)T * (H / 128) * 4, cudaMemcpyHostToDevice, s) ||
+        cudaMemcpyAsync(c->ws + L.st_xsf, h_x_sf, x_sf_bytes(g, T), cudaMemcpyHostToDevice, s) ||
         cudaMemcpyAsync(c->ws + L.st_idx, h_topk_idx, (size_t)T * k * 4, cudaMemcpyHostToDevice, s) ||
         cudaMemcpyAsync(c->ws + L.st_w, h_topk_weights, (size_t)T * k * 4, cudaMemcpyHostToDevice, s))
         return MOE_ERR_CUDA;
@@ -335,7 +400,7 @@ int moe_get_dispatch(moe_ctx *c, int32_t *counts, int32_t *offsets, int32_t *gat
     return MOE_OK;
 }
 
-int moe_get_intermediates(moe_ctx *c, void *l2_acts, float *l2_sf, void *l2_out, void *stream) {
+int moe_get_intermediates(moe_ctx *c, void *l2_acts, void *l2_sf, void *l2_out, void *stream) {
     if (!c) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t H = c->cfg.hidden, I = c->cfg.inter;
@@ -344,9 +409,14 @@ int moe_get_intermediates(moe_ctx *c, void *l2_acts, float *l2_sf, void *l2_out,
     if (!P) return MOE_OK;
     if (l2_acts && cudaMemcpyAsync(l2_acts, c->ws + c->L.l2_acts, P * I, cudaMemcpyDeviceToDevice, s))
         return MOE_ERR_CUDA;
-    if (l2_sf && cudaMemcpy2DAsync(l2_sf, P * 4, c->ws + c->L.l2_sf, Pm * 4, P * 4, I / 64,
-                                   cudaMemcpyDeviceToDevice, s))
-        return MOE_ERR_CUDA;
+    if (l2_sf) {
+        const cudaError_t e =
+            c->cfg.wfmt == MOE_W_FP8_BLK128
+                ? cudaMemcpy2DAsync(l2_sf, P * 4, c->ws + c->L.l2_sf, Pm * 4, P * 4, I / 64,
+                                    cudaMemcpyDeviceToDevice, s)
+                : cudaMemcpyAsync(l2_sf, c->ws + c->L.l2_sf, P * (I / 32), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
     if (l2_out && cudaMemcpyAsync(l2_out, c->ws + c->L.l2_out, P * H * 2, cudaMemcpyDeviceToDevice, s))
         return MOE_ERR_CUDA;
     return MOE_OK;

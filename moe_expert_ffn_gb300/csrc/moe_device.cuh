@@ -157,6 +157,21 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= A . B^T with per-32-K UE8M0 scales applied by the tensor core
+// (kind::mxf8f6f4, one scale per row per K=32 step).  The scale words live
+// in TMEM at sfa/sfb; the instruction descriptor selects their byte.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -195,6 +210,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Four consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
+                 "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -211,6 +237,15 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
     return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with A = E4M3, B = E2M1, both
+// K-major, D = FP32, UE8M0 scales; sf_id selects byte sf_id of each scale
+// word (the scale of K step sf_id of a 128-K stage).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_e2m1(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4) | (0u << 7) | (5u << 10) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+           (static_cast<uint32_t>(sf_id) << 29);
 }
 
 // Instruction descriptor: kind::f8f6f4, A = B = E4M3, both K-major, D = FP32.

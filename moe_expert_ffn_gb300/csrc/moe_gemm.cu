@@ -32,6 +32,7 @@
 // epilogue keeps 128 (L1) or 64 (L2) accumulators and loads TMEM in small
 // pieces so nothing spills.
 #include "moe_device.cuh"
+#include "moe_gemm_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -73,50 +74,6 @@ constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
 constexpr size_t kL1SmemBytes = 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes;
 constexpr size_t kL2SmemBytes = 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes;
-
-struct Tile {
-    int e, row0, rows, nb, nmb;   // nmb: M blocks of expert e
-};
-
-// Tile `tile` of a grouped GEMM with NB column blocks: experts in ascending
-// order, each expert's M blocks x NB column blocks walked N-major when the
-// expert has at least kNMajorMinRows pairs (weight tile reused across
-// consecutive CTAs), M-major otherwise (design §12.2 "Auto N-Major").
-__device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__restrict__ offset,
-                                            const int32_t *__restrict__ mb_prefix,
-                                            const int32_t *__restrict__ mblk_expert) {
-    Tile t;
-    const int mbi = tile / NB;
-    const int e = __ldg(mblk_expert + mbi);
-    const int first = __ldg(mb_prefix + e);
-    const int nmb = __ldg(mb_prefix + e + 1) - first;
-    const int off = __ldg(offset + e);
-    const int cnt = __ldg(offset + e + 1) - off;
-    const int local = tile - first * NB;
-    int mb, nb;
-    if (cnt >= kNMajorMinRows) {
-        mb = local % nmb;
-        nb = local / nmb;
-    } else {
-        mb = local / NB;
-        nb = local % NB;
-    }
-    t.e = e;
-    t.row0 = off + mb * kBM;
-    t.rows = min(kBM, cnt - mb * kBM);
-    t.nb = nb;
-    t.nmb = nmb;
-    return t;
-}
-
-__device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
-
-// Bounded wait used only on the abort path (does not look at the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
-}
 
 // Common prologue: barriers, TMEM allocation.  Returns the TMEM base.
 __device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages, int tbufs) {

@@ -1,0 +1,394 @@
+// moe_gemm_fp4.cu -- the grouped GEMMs of the FP4-weight configuration.
+//
+// Weights are FP4 E2M1 (two codes per byte, low nibble = even k) with one
+// UE8M0 scale per 32 K; activations are FP8 E4M3 with one UE8M0 scale per 32
+// K (PR357 Green-Context Split MegaMoE code review, §1 "SM100 FP8/FP4
+// MegaMoE", §6.2 "MXF8F6F4 UMMA"; MegaMoE SM90 Implementation Design (Final),
+// §2.1 "FP4 Tensor Core (E2M1)", "Scale Factor Format").  Both scale kinds are
+// powers of two, so the tensor core applies them itself: tcgen05.mma
+// kind::mxf8f6f4 with block_scale, one scale per row per K=32 step, and the
+// whole K loop accumulates in one TMEM accumulator (no promotion in the
+// epilogue).
+//
+//   L1: h = x . W1^T, then SwiGLU * w and FP8 requantisation with one UE8M0
+//       scale per 32 columns, 2^ceil(log2(amax/448)) (PR357 review §6.1
+//       "SwiGLU/quant"; design §10.1);
+//   L2: o = q . W2^T rounded to BF16 (design §11.1).
+//
+// Weight tiles are loaded by TMA straight from the packed codes: the tensor
+// map type 16U4_ALIGN16B expands every 16 codes (8 bytes) into a 16-byte slot,
+// the layout the f8f6f4 MMA reads for E2M1, so HBM moves half a byte per
+// weight.  Tiles are 128 rows x 128 columns, K stages of 128.  Warp roles, 10
+// warps:
+//   warp 0     TMA producer (6 stages: A 16 KB, B 16 KB);
+//   warp 1     TMEM allocation, then MMA issuer;
+//   warps 2-5  scale writers: for every stage they load the UE8M0 words (four
+//              K steps per 32-bit word) of the tile's 128 A rows and 128 B rows
+//              and tcgen05.st them into a TMEM slot of the scale ring.  The MMA
+//              reads the scale of row r from TMEM lane 32*(m/32) + r%32 (m =
+//              the output row being computed), column base + r/32, so each lane
+//              quadrant holds a full copy: lane 32q + j, column base + c = row
+//              32c + j;
+//   warps 6-9  epilogue, one per TMEM lane quadrant, 128 columns per thread:
+//              two accumulators in TMEM let the next tile's MMAs run while the
+//              epilogue drains the previous one.
+#include "moe_device.cuh"
+#include "moe_gemm_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kBN = 128;
+constexpr int kStages = 6;
+constexpr uint32_t kABytes = kBM * kBK;
+constexpr uint32_t kBBytes = kBN * kBK;                 // E2M1 expanded to one byte per code
+constexpr uint32_t kBTxBytes = kBN * kBK / 2;           // a 16U4 load counts the packed bytes
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAccs = 2;                                // 128-column accumulators
+constexpr uint32_t kSfCol0 = kAccs * kBN;               // scale ring after the accumulators
+constexpr uint32_t kSfSlotCols = 8;                     // 4 columns A scales + 4 columns B scales
+constexpr int kNumSfWarps = 4;
+constexpr int kNumEpiWarps = 4;
+constexpr int kEpiWarp0 = 6;                           // warps 2..5 write scales
+static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM budget");
+
+struct alignas(8) Ctrl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t sf_full[kStages];
+    uint64_t sf_empty[kStages];
+    uint64_t acc_full[kAccs];
+    uint64_t acc_empty[kAccs];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kCtrlBytes = 512;
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl");
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kCtrlBytes;
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const uint32_t *>(p));
+}
+
+// UE8M0 exponent of the smallest power of two 2^e with amax/448 <= 2^e (the
+// ratio in binary32), e in [-127, 127]; -127 for an all-zero group.
+__device__ __forceinline__ int ue8m0_exponent(float amax) {
+    const float r = amax / 448.0f;
+    if (!(r > 0.0f)) return -127;
+    int ex;
+    const float fr = frexpf(r, &ex);
+    int e = (fr == 0.5f) ? ex - 1 : ex;
+    return min(127, max(-127, e));
+}
+
+template <bool kL1, bool kFast, bool kGatherA>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const Fp4Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align1024(raw);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    const int NB = kL1 ? 2 * p.I / kBN : p.H / kBN;
+    const int KB = kL1 ? p.H / kBK : p.I / kBK;
+    const int brow0 = kL1 ? 2 * p.I : p.H;          // B rows per expert
+    const int sf_row_bytes = (kL1 ? p.H : p.I) / 32; // scale bytes per row of A and B
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctrl->full[s]), 1);
+            mbar_init(smem_u32(&ctrl->empty[s]), 1);
+            mbar_init(smem_u32(&ctrl->sf_full[s]), kNumSfWarps);
+            mbar_init(smem_u32(&ctrl->sf_empty[s]), 1);
+        }
+        for (int b = 0; b < kAccs; ++b) {
+            mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
+            mbar_init(smem_u32(&ctrl->acc_empty[b]), kNumEpiWarps);
+        }
+        ctrl->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    volatile int *abort_flag = &ctrl->abort;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        const uint64_t pol_once = policy_evict_first();
+        const uint64_t pol_shared = policy_evict_normal();
+        const uint64_t pol_a = policy_evict_last();
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
+            int tok[4] = {0, 0, 0, 0};
+            if (kGatherA) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = (int)lane * 4 + i;
+                    tok[i] = r < t.rows ? __ldg(p.gather + t.row0 + r) / p.k : 0;
+                }
+            }
+            const int n_g4 = (t.rows + 3) >> 2;
+            const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : kABytes) + kBTxBytes;
+            const int brow = t.e * brow0 + t.nb * kBN;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = smem_u32(&ctrl->full[s]);
+                if (lane == 0) mbar_arrive_expect_tx(full, tx);
+                __syncwarp();
+                if (kGatherA) {
+                    if ((int)lane < n_g4)
+                        tma_gather4(base + s * kStageBytes + lane * 512, &tm_a, kb * kBK, tok[0], tok[1],
+                                    tok[2], tok[3], full, pol_a);
+                } else if (lane == 0) {
+                    tma_load_2d(base + s * kStageBytes, &tm_a, kb * kBK, t.row0, full, pol_a);
+                }
+                if (lane == 0)
+                    tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, kb * kBK, brow, full, pol_w);
+            }
+        }
+        if (!ok)
+            for (int i = max(0, it - kStages); i < it; ++i)
+                drain_wait(smem_u32(&ctrl->full[i % kStages]), (i / kStages) & 1);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        int it = 0, tc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
+            const int b = tc % kAccs;
+            if (!mbar_wait(smem_u32(&ctrl->acc_empty[b]), ((tc / kAccs) & 1) ^ 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
+                    !mbar_wait(smem_u32(&ctrl->sf_full[s]), ph, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t ad = sw128_kmajor_desc(base + s * kStageBytes);
+                    const uint64_t bd = sw128_kmajor_desc(base + s * kStageBytes + kABytes);
+                    const uint32_t sfa = tmem + kSfCol0 + s * kSfSlotCols;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk)
+                        umma_mx(tmem + b * kBN, ad + 2 * kk, bd + 2 * kk, idesc_mx_e4m3_e2m1(kBM, kBN, kk),
+                                sfa, sfa + 4, (kb | kk) != 0);
+                    umma_commit(smem_u32(&ctrl->empty[s]));
+                    umma_commit(smem_u32(&ctrl->sf_empty[s]));
+                    if (kb == KB - 1) umma_commit(smem_u32(&ctrl->acc_full[b]));
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && it > 0)
+            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1);
+    } else if (warp < kEpiWarp0) {
+        // ---------------- scale writers ----------------
+        const int q = warp & 3;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + kSfCol0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            // row c*32 + lane of the tile, for c = 0..3 (A: pool rows, B: weight rows)
+            const uint8_t *arow[4];
+            const uint8_t *brow[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int r = 32 * c + (int)lane;
+                const int prow = t.row0 + min(r, t.rows - 1);   // masked rows reuse a valid row
+                if (kL1)
+                    arow[c] = p.a_sf + (size_t)(__ldg(p.gather + prow) / p.k) * sf_row_bytes;
+                else
+                    arow[c] = p.a_sf + (size_t)prow * sf_row_bytes;
+                brow[c] = p.b_sf + (size_t)(t.e * brow0 + t.nb * kBN + r) * sf_row_bytes;
+            }
+            uint32_t wa[4], wb[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                wa[c] = ld_u32(arow[c]);
+                wb[c] = ld_u32(brow[c]);
+            }
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                // words of the next K block, loaded while this one is stored
+                uint32_t na[4], nbw[4];
+                const int kn = min(kb + 1, KB - 1) * 4;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    na[c] = ld_u32(arow[c] + kn);
+                    nbw[c] = ld_u32(brow[c] + kn);
+                }
+                if (!mbar_wait(smem_u32(&ctrl->sf_empty[s]), ph ^ 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = t_lane + s * kSfSlotCols;
+                tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
+                tmem_st4(col + 4, wb[0], wb[1], wb[2], wb[3]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctrl->sf_full[s]));
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    wa[c] = na[c];
+                    wb[c] = nbw[c];
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;
+        const int lrow = q * 32 + (int)lane;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        int tc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
+            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            const int b = tc % kAccs;
+            if (!mbar_wait(smem_u32(&ctrl->acc_full[b]), (tc / kAccs) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool valid = lrow < t.rows;
+            const bool warp_on = q * 32 < t.rows;
+            float acc[128];
+            if (warp_on) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32(t_lane + b * kBN + 32 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * c + i] = v[i];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[b]));
+            if (!valid) continue;
+            const int row = t.row0 + lrow;
+            if (kL1) {
+                // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
+                const float wgt = __ldg(p.topk_w + __ldg(p.gather + row));
+                const float clampv = p.clamp;
+#pragma unroll
+                for (int o = 0; o < 64; ++o) {
+                    const int gi = 16 * (o >> 3) + (o & 7);
+                    const float g = fminf(fmaxf(acc[gi], -clampv), clampv);
+                    const float u = fminf(fmaxf(acc[gi + 8], -clampv), clampv);
+                    float silu;
+                    if (kFast)
+                        silu = __fdividef(g, 1.0f + __expf(-g));
+                    else
+                        silu = g / (1.0f + expf(-g));
+                    acc[gi] = silu * u * wgt;
+                }
+                // two 32-column groups, UE8M0 scale 2^ceil(log2(amax/448)) each
+                uint32_t pk[16];
+                uint32_t codes = 0;
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp) {
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int o = 32 * grp; o < 32 * grp + 32; ++o)
+                        amax = fmaxf(amax, fabsf(acc[16 * (o >> 3) + (o & 7)]));
+                    const int e = ue8m0_exponent(amax);
+                    const float sf = ldexpf(1.0f, e);
+                    codes |= static_cast<uint32_t>(e + 127) << (8 * grp);
+#pragma unroll
+                    for (int w4 = 8 * grp; w4 < 8 * grp + 8; ++w4) {
+                        float qv[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int o = w4 * 4 + j;
+                            const float a = acc[16 * (o >> 3) + (o & 7)];
+                            qv[j] = (amax == 0.0f) ? 0.0f : __fdiv_rn(a, sf);
+                        }
+                        pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
+                    }
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.I + t.nb * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                *reinterpret_cast<uint16_t *>(p.l2_sf + (size_t)row * (p.I / 32) + 2 * t.nb) =
+                    static_cast<uint16_t>(codes);
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + t.nb * kBN);
+#pragma unroll
+                for (int v = 0; v < 16; ++v)
+                    dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]), bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                                        bf16x2(acc[8 * v + 4], acc[8 * v + 5]), bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool kL1, bool kFast, bool kGatherA>
+void launch_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Fp4Params &p, int num_sms,
+              cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(fp4_gemm_kernel<kL1, kFast, kGatherA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        configured = true;
+    }
+    fp4_gemm_kernel<kL1, kFast, kGatherA><<<num_sms, kThreads, kSmemBytes, s>>>(tm_a, tm_b, p);
+}
+
+}  // namespace
+
+void launch_fp4_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
+                   int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+    if (fast_math) {
+        if (gather_a) launch_t<true, true, true>(tm_a, tm_w1, p, num_sms, s);
+        else launch_t<true, true, false>(tm_a, tm_w1, p, num_sms, s);
+    } else {
+        if (gather_a) launch_t<true, false, true>(tm_a, tm_w1, p, num_sms, s);
+        else launch_t<true, false, false>(tm_a, tm_w1, p, num_sms, s);
+    }
+}
+
+void launch_fp4_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
+                   cudaStream_t s) {
+    launch_t<false, false, false>(tm_a, tm_w2, p, num_sms, s);
+}
+
+}  // namespace moe

@@ -61,6 +61,30 @@ struct L2Params {
 void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
                cudaStream_t s);
 
+// FP4-weight configuration: both GEMMs with UE8M0 block scales applied by the
+// tensor core (moe_gemm_fp4.cu).
+struct Fp4Params {
+    const int32_t *gather, *offset, *mb_prefix, *mblk_expert;
+    const uint8_t *a_sf;      // L1: x scales u8 [T, H/32]; L2: l2 act scales u8 [Pmax, I/32]
+    const uint8_t *b_sf;      // L1: W1 scales u8 [E*2I, H/32] (interleaved rows); L2: u8 [E*H, I/32]
+    const float *topk_w;      // [T*k] (L1)
+    uint8_t *l2_acts;         // [Pmax, I] (L1 output)
+    uint8_t *l2_sf;           // u8 [Pmax, I/32] (L1 output)
+    uint16_t *l2_out;         // bf16 [Pmax, H] (L2 output)
+    int *err;
+    int H, I, E, k, Pmax;
+    float clamp;
+};
+void launch_fp4_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
+                   int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+void launch_fp4_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
+                   cudaStream_t s);
+
+// FP4 weight transform: W1 packed rows and their UE8M0 scale rows interleaved
+// like the FP8 rows (row bytes given), W2 copied by the caller.
+void launch_interleave_rows(const uint8_t *src, uint8_t *dst, int E, int I, int row_bytes,
+                            cudaStream_t s);
+
 // Combine: y[t] = bf16( sum_j bf16 l2_out[pair_pool[t*k+j]] ) in slot order.
 void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int k, int H,
                     uint16_t *y, cudaStream_t s);

@@ -8,24 +8,27 @@
 // interleaved 128-row block j holds gate rows [64j, 64j+64) and up rows
 // [I+64j, I+64j+64): its scales are the pair (gate block j/2, up block
 // I/128 + j/2) of the canonical [E, 2I/128, H/128] scale array (design §15.2).
-// W2 and its scales keep the canonical layout.
+// W2 and its scales keep the canonical layout.  In the FP4-weight format the
+// same row order applies to the packed E2M1 rows and to their per-32 UE8M0
+// scale rows.
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 namespace {
 
-__global__ void interleave_w1_kernel(const uint8_t *__restrict__ w1, uint8_t *__restrict__ w1i,
-                                     int rows_total, int H, int I) {
-    const int vecs = H / 16;
+// Rows of [E, 2I, row_bytes] in the interleaved order; row_bytes % 4 == 0.
+__global__ void interleave_rows_kernel(const uint8_t *__restrict__ src_rows, uint8_t *__restrict__ dst_rows,
+                                       int rows_total, int row_bytes, int I) {
+    const int words = row_bytes / 4;
     for (int row = blockIdx.x; row < rows_total; row += gridDim.x) {
         const int e = row / (2 * I);
         const int r = row - e * 2 * I;
         const int g = r >> 4, m = r & 15;
         const int src = (m < 8) ? (8 * g + m) : (I + 8 * g + m - 8);
-        const uint4 *s = reinterpret_cast<const uint4 *>(w1 + ((size_t)e * 2 * I + src) * H);
-        uint4 *d = reinterpret_cast<uint4 *>(w1i + (size_t)row * H);
-        for (int v = threadIdx.x; v < vecs; v += blockDim.x) d[v] = s[v];
+        const uint32_t *s = reinterpret_cast<const uint32_t *>(src_rows + ((size_t)e * 2 * I + src) * row_bytes);
+        uint32_t *d = reinterpret_cast<uint32_t *>(dst_rows + (size_t)row * row_bytes);
+        for (int v = threadIdx.x; v < words; v += blockDim.x) d[v] = s[v];
     }
 }
 
@@ -48,9 +51,15 @@ __global__ void interleave_w1_sf_kernel(const float *__restrict__ sf, float2 *__
 void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, float2 *w1i_sf, int E,
                          int H, int I, cudaStream_t s) {
     const int rows = E * 2 * I;
-    interleave_w1_kernel<<<min(rows, 65535), 256, 0, s>>>(w1, w1i, rows, H, I);
+    interleave_rows_kernel<<<min(rows, 65535), 256, 0, s>>>(w1, w1i, rows, H, I);
     const int n = E * (2 * I / 128) * (H / 128);
     interleave_w1_sf_kernel<<<min((n + 255) / 256, 4096), 256, 0, s>>>(w1_sf, w1i_sf, E, H, I);
+}
+
+void launch_interleave_rows(const uint8_t *src, uint8_t *dst, int E, int I, int row_bytes,
+                            cudaStream_t s) {
+    const int rows = E * 2 * I;
+    interleave_rows_kernel<<<min(rows, 65535), 128, 0, s>>>(src, dst, rows, row_bytes, I);
 }
 
 }  // namespace moe

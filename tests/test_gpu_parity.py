@@ -177,3 +177,53 @@ def test_full_size_sampled_tokens(m, orc, name):
     rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, name)
     print(f"{name}: sampled tokens {tokens.tolist()} rel L2 {rel:.2e} max/rms {mx:.2e}")
     assert torch.isfinite(y.float()).all()
+
+
+FP4 = [
+    moe_synth.custom(T=40, H=256, I=128, E=8, k=2, seed=61, wfmt=1, name="fp4_tiny"),
+    moe_synth.custom(T=300, H=512, I=384, E=6, k=3, seed=62, wfmt=1, name="fp4_ragged"),
+    moe_synth.custom(T=64, H=384, I=256, E=40, k=4, seed=63, wfmt=1, n_empty=8, name="fp4_sparse"),
+]
+
+
+@pytest.mark.parametrize("wl", FP4, ids=lambda w: w.name)
+def test_fp4_weights_y_matches_oracle(m, orc, wl):
+    inp = moe_synth.make_inputs(wl)
+    _, _, y = _run(m, wl, inp, wfmt=m.MOE_W_FP4_E2M1_UE8M0_32)
+    ref = bf16_bits_to_float(orc.forward(inp, wfmt=1))
+    rel, mx = assert_y_close(y, ref, wl.name)
+    print(f"{wl.name}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
+
+
+def test_fp4_l2_activations_stage_by_stage(m, orc):
+    wl = moe_synth.custom(T=48, H=256, I=256, E=4, k=2, seed=64, wfmt=1)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, _ = _run(m, wl, inp, wfmt=m.MOE_W_FP4_E2M1_UE8M0_32)
+    _, offsets, gather = layer.get_dispatch(wl.T)
+    acts, sf, out = layer.get_intermediates(wl.T)
+    acts, sf, gather = acts.cpu().numpy(), sf.cpu().numpy(), gather.cpu().numpy()
+    idx, w = inp["topk_idx"].numpy(), inp["topk_weights"].numpy()
+    mism = total = 0
+    for r in range(0, int(offsets[-1]), 5):
+        t, j = divmod(int(gather[r]), wl.k)
+        pr = orc.pair(inp, t, int(idx[t, j]), float(w[t, j]), wfmt=1)
+        assert np.array_equal(sf[r].astype(np.float32), pr["sf"]), r      # UE8M0 codes
+        mism += int((acts[r] != pr["q"]).sum())
+        total += wl.I
+    assert mism <= 0.01 * total, (mism, total)
+
+
+def test_fp4_full_size_sampled_tokens(m, orc):
+    wl = moe_synth.WORKLOADS["fp4"]
+    inp = moe_synth.make_inputs(wl, device=DEV)
+    layer = new_layer(m, wl, DEV, wfmt=m.MOE_W_FP4_E2M1_UE8M0_32)
+    layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    y = layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    counts, _, _ = layer.get_dispatch(wl.T)
+    assert (counts.cpu().numpy() == 0).sum() >= wl.n_empty
+    tokens = np.sort(np.random.default_rng(9).choice(wl.T, size=6, replace=False)).astype(np.int32)
+    ref = bf16_bits_to_float(orc.forward(sub_inputs(inp, tokens), wfmt=1))
+    rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, "fp4")
+    print(f"fp4: rel L2 {rel:.2e} max/rms {mx:.2e}")
