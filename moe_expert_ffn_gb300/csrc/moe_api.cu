@@ -143,7 +143,8 @@ struct moe_ctx {
     uint8_t *wt;
     bool weights_ready;
     int last_T;
-    CUtensorMap tm_w1, tm_w2, tm_l2a, tm_pool;
+    CUtensorMap tm_w1, tm_w2;
+    AMaps tm_l2a, tm_pool;
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
     int prof_max, prof_n;
@@ -189,8 +190,12 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
                          make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I / 2, 128, 128, packed)
                    : make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
                          make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128)) &&
-              make_map(&c->tm_l2a, c->ws + c->L.l2_acts, I, Pm, I, 128, 128) &&
-              make_map(&c->tm_pool, c->ws + c->L.pool, H, Pm, H, 128, 128);
+              make_map(&c->tm_l2a.box[0], c->ws + c->L.l2_acts, I, Pm, I, 128, 32) &&
+              make_map(&c->tm_l2a.box[1], c->ws + c->L.l2_acts, I, Pm, I, 128, 64) &&
+              make_map(&c->tm_l2a.box[2], c->ws + c->L.l2_acts, I, Pm, I, 128, 128) &&
+              make_map(&c->tm_pool.box[0], c->ws + c->L.pool, H, Pm, H, 128, 32) &&
+              make_map(&c->tm_pool.box[1], c->ws + c->L.pool, H, Pm, H, 128, 64) &&
+              make_map(&c->tm_pool.box[2], c->ws + c->L.pool, H, Pm, H, 128, 128);
     if (!ok) {
         free(c);
         return MOE_ERR_CUDA;
@@ -279,9 +284,10 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     // A operand: gather token rows in the L1 producer (tile::gather4) when the
     // M blocks are sparse, else copy them once into the pool
     const bool gather_a = c->l1_a_mode ? c->l1_a_mode == 1 : (long long)T * k <= 4LL * E;
-    CUtensorMap tm_x;
+    AMaps tm_x;
     if (gather_a) {
-        if (!make_map(&tm_x, x, (uint64_t)H, (uint64_t)T, (uint64_t)H, 128, 1)) return MOE_ERR_CUDA;
+        if (!make_map(&tm_x.box[0], x, (uint64_t)H, (uint64_t)T, (uint64_t)H, 128, 1)) return MOE_ERR_CUDA;
+        tm_x.box[1] = tm_x.box[2] = tm_x.box[0];
     } else {
         launch_pool_gather(static_cast<const uint8_t *>(x), o.gather, o.offset + E, k, H, T * k,
                            c->w<uint8_t>(L.pool), s);

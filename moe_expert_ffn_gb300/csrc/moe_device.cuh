@@ -97,6 +97,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// Prefetch a 2-D box into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(x),
+                 "r"(y)
+                 : "memory");
+}
+
 // Four rows r0..r3 of a 2-D tensor (box one row high) into four consecutive
 // box-sized slots of shared memory.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *tm, int x, int r0,

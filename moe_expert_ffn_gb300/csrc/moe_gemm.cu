@@ -163,7 +163,7 @@ __device__ __forceinline__ void promote_l2(float (&acc)[64], uint32_t tcol, floa
 // the dispatch step (tm_a = pool, 128-row boxes).
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
-    l1_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w1,
+    l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
               const L1Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = __ldg(p.mb_prefix + p.E) * NB;
 
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_a.box[0]);
+        tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_w1);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs);
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // gather4: only the requests that carry valid rows; the other smem
             // rows keep stale bytes, which reach only masked accumulator rows
             const int n_g4 = (t.rows + 3) >> 2;
-            const uint32_t tx = kGatherA ? (uint32_t)n_g4 * 4 * kBK + kL1BBytes : kL1StageBytes;
+            const int abox = a_box_index(t.rows);
+            const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : (32u << abox) * kBK) + kL1BBytes;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kL1Stages;
                 const uint32_t ph = (it / kL1Stages) & 1;
@@ -220,10 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (kGatherA) {
                     if ((int)lane < n_g4)
-                        tma_gather4(base + s * kL1StageBytes + lane * 512, &tm_a, kb * kBK, tok[0],
+                        tma_gather4(base + s * kL1StageBytes + lane * 512, &tm_a.box[0], kb * kBK, tok[0],
                                     tok[1], tok[2], tok[3], full, pol_x);
                 } else if (lane == 0) {
-                    tma_load_2d(base + s * kL1StageBytes, &tm_a, kb * kBK, t.row0, full, pol_x);
+                    tma_load_2d(base + s * kL1StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_x);
                 }
                 if (lane == 0)
                     tma_load_2d(base + s * kL1StageBytes + kL1ABytes, &tm_w1, kb * kBK, wrow, full,
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // L2: down GEMM with per-64 activation scales, BF16 output in pool order
 // ============================================================================
 __global__ void __launch_bounds__(kThreads, 1)
-    l2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w2,
+    l2_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w2,
               const L2Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -369,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = __ldg(p.mb_prefix + p.E) * NB;
 
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_a.box[0]);
+        tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_w2);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs);
@@ -394,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t full = smem_u32(&ctrl->full[s]);
-                    mbar_arrive_expect_tx(full, kL2StageBytes);
-                    tma_load_2d(base + s * kL2StageBytes, &tm_a, kb * kBK, t.row0, full, pol_a);
+                    const int abox = a_box_index(t.rows);
+                    mbar_arrive_expect_tx(full, (32u << abox) * kBK + kL2BBytes);
+                    tma_load_2d(base + s * kL2StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_a);
                     tma_load_2d(base + s * kL2StageBytes + kL2ABytes, &tm_w2, kb * kBK, wrow, full,
                                 pol_w);
                 }
@@ -508,7 +512,7 @@ size_t l1_smem_bytes() { return kL1SmemBytes; }
 size_t l2_smem_bytes() { return kL2SmemBytes; }
 
 template <bool kFast, bool kGatherA>
-static void launch_l1_t(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
+static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
                         int num_sms, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
@@ -519,7 +523,7 @@ static void launch_l1_t(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const
     l1_kernel<kFast, kGatherA><<<num_sms, kThreads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
 }
 
-void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
+void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
                bool gather_a, int num_sms, cudaStream_t s) {
     if (fast_math) {
         if (gather_a) launch_l1_t<true, true>(tm_a, tm_w1, p, num_sms, s);
@@ -530,7 +534,7 @@ void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params
     }
 }
 
-void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
+void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
                cudaStream_t s) {
     static bool configured = false;
     if (!configured) {

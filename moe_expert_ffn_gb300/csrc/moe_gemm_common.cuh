@@ -44,6 +44,9 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__r
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
+// Index of the smallest A box (32, 64 or 128 rows) covering `rows` rows.
+__device__ __forceinline__ int a_box_index(int rows) { return rows <= 32 ? 0 : (rows <= 64 ? 1 : 2); }
+
 // Bounded wait used only on the abort path (does not look at the abort flag).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();

@@ -86,7 +86,7 @@ __device__ __forceinline__ int ue8m0_exponent(float amax) {
 
 template <bool kL1, bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
-    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+    fp4_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const Fp4Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ctrl->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_a.box[0]);
+        tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_b);
     }
     if (warp == 1) {
@@ -146,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const int n_g4 = (t.rows + 3) >> 2;
-            const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : kABytes) + kBTxBytes;
+            const int abox = a_box_index(t.rows);
+            const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : (32u << abox) * kBK) + kBTxBytes;
             const int brow = t.e * brow0 + t.nb * kBN;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kStages;
@@ -160,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (kGatherA) {
                     if ((int)lane < n_g4)
-                        tma_gather4(base + s * kStageBytes + lane * 512, &tm_a, kb * kBK, tok[0], tok[1],
+                        tma_gather4(base + s * kStageBytes + lane * 512, &tm_a.box[0], kb * kBK, tok[0], tok[1],
                                     tok[2], tok[3], full, pol_a);
                 } else if (lane == 0) {
-                    tma_load_2d(base + s * kStageBytes, &tm_a, kb * kBK, t.row0, full, pol_a);
+                    tma_load_2d(base + s * kStageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_a);
                 }
                 if (lane == 0)
                     tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, kb * kBK, brow, full, pol_w);
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kL1, bool kFast, bool kGatherA>
-void launch_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Fp4Params &p, int num_sms,
+void launch_t(const AMaps &tm_a, const CUtensorMap &tm_b, const Fp4Params &p, int num_sms,
               cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
@@ -375,7 +377,7 @@ void launch_t(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const Fp4Params 
 
 }  // namespace
 
-void launch_fp4_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
+void launch_fp4_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
                    int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
     if (fast_math) {
         if (gather_a) launch_t<true, true, true>(tm_a, tm_w1, p, num_sms, s);
@@ -386,7 +388,7 @@ void launch_fp4_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const Fp4P
     }
 }
 
-void launch_fp4_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
+void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
                    cudaStream_t s) {
     launch_t<false, false, false>(tm_a, tm_w2, p, num_sms, s);
 }

@@ -12,6 +12,14 @@ constexpr int kBM = 128;   // pool rows (routed pairs) per M block
 constexpr int kBK = 128;   // K bytes per pipeline stage (one scale block)
 constexpr int kNMajorMinRows = 256;  // experts with at least this many pairs walk N-major
 
+// Tensor maps of an A operand (rows of 128 bytes): with tile::gather4 the
+// first map covers x [T, H] with one-row boxes; otherwise box[i] covers the
+// pool / L2 activations [Pmax, K] with boxes of 32 << i rows, and a tile loads
+// the smallest box that covers its valid rows.
+struct AMaps {
+    CUtensorMap box[3];
+};
+
 // Dispatch result: where the pairs of each expert sit in the pool.
 struct DispatchOut {
     int32_t *count;        // [E]
@@ -41,7 +49,7 @@ struct L1Params {
 };
 // gather_a: tm_a maps x [T, H] with one-row boxes (rows gathered in the
 // kernel); otherwise tm_a maps the pool [Pmax, H] with 128-row boxes.
-void launch_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
+void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
                bool gather_a, int num_sms, cudaStream_t s);
 
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
@@ -58,7 +66,7 @@ struct L2Params {
     int *err;
     int H, I, E, Pmax;
 };
-void launch_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
+void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
                cudaStream_t s);
 
 // FP4-weight configuration: both GEMMs with UE8M0 block scales applied by the
@@ -75,9 +83,9 @@ struct Fp4Params {
     int H, I, E, k, Pmax;
     float clamp;
 };
-void launch_fp4_l1(const CUtensorMap &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
+void launch_fp4_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
                    int fast_math, bool gather_a, int num_sms, cudaStream_t s);
-void launch_fp4_l2(const CUtensorMap &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
+void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
                    cudaStream_t s);
 
 // FP4 weight transform: W1 packed rows and their UE8M0 scale rows interleaved
