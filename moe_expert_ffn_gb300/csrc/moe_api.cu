@@ -15,9 +15,16 @@ namespace {
 
 constexpr size_t kAlign = 1024;
 
+// Row pitch padding of the row-major operands the GEMMs read with TMA: rows
+// of a 2^k-byte pitch put every row of a tile (and the same K offset of all
+// concurrent tiles) on the same few memory partitions; one extra 128-byte
+// segment per row spreads them.
+constexpr size_t kPitchPad = 128;
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
+    size_t pool_pitch, acts_pitch, w1_pitch, w2_pitch;   // bytes per row
     // workspace
     size_t err, count, offset, mb_prefix, mblk_expert, gather, pair_pool;
     size_t pool, l2_acts, l2_sf, l2_out;
@@ -48,6 +55,11 @@ Layout make_layout(const moe_config *c) {
     const size_t Tm = c->max_tokens, k = c->topk, E = c->num_experts, H = c->hidden, I = c->inter;
     const size_t Pm = Tm * k;
     const size_t MBmax = Pm / kBM + E + 1;
+    const bool fp4 = c->wfmt == MOE_W_FP4_E2M1_UE8M0_32;
+    L.pool_pitch = H + kPitchPad;
+    L.acts_pitch = I + kPitchPad;
+    L.w1_pitch = (fp4 ? H / 2 : H) + (fp4 ? kPitchPad / 2 : kPitchPad);
+    L.w2_pitch = (fp4 ? I / 2 : I) + (fp4 ? kPitchPad / 2 : kPitchPad);
     size_t o = 0;
     auto take = [&](size_t bytes, size_t align) {
         o = align_up(o, align);
@@ -62,8 +74,8 @@ Layout make_layout(const moe_config *c) {
     L.mblk_expert = take(4 * MBmax, 256);
     L.gather = take(4 * Pm, 256);
     L.pair_pool = take(4 * Pm, 256);
-    L.pool = take(Pm * H, kAlign);
-    L.l2_acts = take(Pm * I, kAlign);
+    L.pool = take(Pm * L.pool_pitch, kAlign);
+    L.l2_acts = take(Pm * L.acts_pitch, kAlign);
     L.l2_sf = take(4 * (I / 64) * Pm, kAlign);
     L.l2_out = take(2 * Pm * H, kAlign);
     L.st_x = take(Tm * H, kAlign);
@@ -74,15 +86,15 @@ Layout make_layout(const moe_config *c) {
     L.ws_total = align_up(o, kAlign);
 
     o = 0;
-    if (c->wfmt == MOE_W_FP8_BLK128) {
-        L.w1i = take(E * 2 * I * H, kAlign);
+    if (!fp4) {
+        L.w1i = take(E * 2 * I * L.w1_pitch, kAlign);
         L.w1i_sf = take(8 * E * (2 * I / 128) * (H / 128), 256);
-        L.w2 = take(E * H * I, kAlign);
+        L.w2 = take(E * H * L.w2_pitch, kAlign);
         L.w2_sf = take(4 * E * (H / 128) * (I / 128), 256);
     } else {   // packed E2M1 rows and per-32 UE8M0 scale rows
-        L.w1i = take(E * 2 * I * H / 2, kAlign);
+        L.w1i = take(E * 2 * I * L.w1_pitch, kAlign);
         L.w1i_sf = take(E * 2 * I * H / 32, 256);
-        L.w2 = take(E * H * I / 2, kAlign);
+        L.w2 = take(E * H * L.w2_pitch, kAlign);
         L.w2_sf = take(E * H * I / 32, 256);
     }
     L.wt_total = align_up(o, kAlign);
@@ -186,16 +198,14 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     const uint64_t Pm = (uint64_t)g.max_tokens * g.topk;
     const bool fp4 = g.wfmt == MOE_W_FP4_E2M1_UE8M0_32;
     const CUtensorMapDataType packed = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
-    bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H / 2, 128, 128, packed) &&
-                         make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I / 2, 128, 128, packed)
-                   : make_map(&c->tm_w1, c->wt + c->L.w1i, H, E * 2 * I, H, 128, 256) &&
-                         make_map(&c->tm_w2, c->wt + c->L.w2, I, E * H, I, 128, 128)) &&
-              make_map(&c->tm_l2a.box[0], c->ws + c->L.l2_acts, I, Pm, I, 128, 32) &&
-              make_map(&c->tm_l2a.box[1], c->ws + c->L.l2_acts, I, Pm, I, 128, 64) &&
-              make_map(&c->tm_l2a.box[2], c->ws + c->L.l2_acts, I, Pm, I, 128, 128) &&
-              make_map(&c->tm_pool.box[0], c->ws + c->L.pool, H, Pm, H, 128, 32) &&
-              make_map(&c->tm_pool.box[1], c->ws + c->L.pool, H, Pm, H, 128, 64) &&
-              make_map(&c->tm_pool.box[2], c->ws + c->L.pool, H, Pm, H, 128, 128);
+    const Layout &L = c->L;
+    bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128, packed) &&
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128, packed)
+                   : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128));
+    for (int i = 0; ok && i < 3; ++i)
+        ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
+             make_map(&c->tm_pool.box[i], c->ws + L.pool, H, Pm, L.pool_pitch, 128, 32u << i);
     if (!ok) {
         free(c);
         return MOE_ERR_CUDA;
@@ -227,10 +237,11 @@ int moe_transform_weights(moe_ctx *c, const void *w1, const void *w1_sf, const v
         if (!aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1_sf, 4) || !aligned(w2_sf, 4))
             return MOE_ERR_INVALID_ARG;
         launch_interleave_rows(static_cast<const uint8_t *>(w1), c->wt_at<uint8_t>(c->L.w1i), (int)E,
-                               (int)I, (int)(H / 2), s);
+                               (int)I, (int)(H / 2), (int)c->L.w1_pitch, s);
         launch_interleave_rows(static_cast<const uint8_t *>(w1_sf), c->wt_at<uint8_t>(c->L.w1i_sf), (int)E,
-                               (int)I, (int)(H / 32), s);
-        if (cudaMemcpyAsync(c->wt + c->L.w2, w2, E * H * I / 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+                               (int)I, (int)(H / 32), (int)(H / 32), s);
+        if (cudaMemcpy2DAsync(c->wt + c->L.w2, c->L.w2_pitch, w2, I / 2, I / 2, E * H,
+                              cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(c->wt + c->L.w2_sf, w2_sf, E * H * I / 32, cudaMemcpyDeviceToDevice, s) !=
                 cudaSuccess)
             return MOE_ERR_CUDA;
@@ -239,9 +250,10 @@ int moe_transform_weights(moe_ctx *c, const void *w1, const void *w1_sf, const v
         return MOE_OK;
     }
     launch_transform_w1(static_cast<const uint8_t *>(w1), static_cast<const float *>(w1_sf),
-                        c->wt_at<uint8_t>(c->L.w1i), c->wt_at<float2>(c->L.w1i_sf), (int)E, (int)H,
-                        (int)I, s);
-    if (cudaMemcpyAsync(c->wt + c->L.w2, w2, E * H * I, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+                        c->wt_at<uint8_t>(c->L.w1i), (int)c->L.w1_pitch, c->wt_at<float2>(c->L.w1i_sf),
+                        (int)E, (int)H, (int)I, s);
+    if (cudaMemcpy2DAsync(c->wt + c->L.w2, c->L.w2_pitch, w2, I, I, E * H, cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     if (cudaMemcpyAsync(c->wt + c->L.w2_sf, w2_sf, 4 * E * (H / 128) * (I / 128),
                         cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -290,7 +302,7 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
         tm_x.box[1] = tm_x.box[2] = tm_x.box[0];
     } else {
         launch_pool_gather(static_cast<const uint8_t *>(x), o.gather, o.offset + E, k, H, T * k,
-                           c->w<uint8_t>(L.pool), s);
+                           c->w<uint8_t>(L.pool), (int)L.pool_pitch, s);
     }
 
     if (g.wfmt == MOE_W_FP4_E2M1_UE8M0_32) {
@@ -303,6 +315,7 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
         f.b_sf = c->wt_at<uint8_t>(L.w1i_sf);
         f.topk_w = topk_weights;
         f.l2_acts = c->w<uint8_t>(L.l2_acts);
+        f.acts_pitch = (int)L.acts_pitch;
         f.l2_sf = c->w<uint8_t>(L.l2_sf);
         f.l2_out = c->w<uint16_t>(L.l2_out);
         f.err = o.err;
@@ -334,6 +347,7 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     p1.topk_w = topk_weights;
     p1.w1_sf = c->wt_at<float2>(L.w1i_sf);
     p1.l2_acts = c->w<uint8_t>(L.l2_acts);
+    p1.acts_pitch = (int)L.acts_pitch;
     p1.l2_sf = c->w<float>(L.l2_sf);
     p1.err = o.err;
     p1.H = H;
@@ -413,7 +427,8 @@ int moe_get_intermediates(moe_ctx *c, void *l2_acts, void *l2_sf, void *l2_out, 
     const size_t P = (size_t)c->last_T * c->cfg.topk;
     const size_t Pm = (size_t)c->cfg.max_tokens * c->cfg.topk;
     if (!P) return MOE_OK;
-    if (l2_acts && cudaMemcpyAsync(l2_acts, c->ws + c->L.l2_acts, P * I, cudaMemcpyDeviceToDevice, s))
+    if (l2_acts && cudaMemcpy2DAsync(l2_acts, I, c->ws + c->L.l2_acts, c->L.acts_pitch, I, P,
+                                     cudaMemcpyDeviceToDevice, s))
         return MOE_ERR_CUDA;
     if (l2_sf) {
         const cudaError_t e =

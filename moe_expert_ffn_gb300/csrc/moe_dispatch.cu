@@ -137,14 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256)
     pool_gather_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ gather,
                        const int32_t *__restrict__ offset_E, int k, int H, int rows_bound,
-                       uint8_t *__restrict__ pool) {
+                       uint8_t *__restrict__ pool, int pool_pitch) {
     const int P = min(__ldg(offset_E), rows_bound);
     const int lane = threadIdx.x & 31;
     const int vecs = H / 16;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < P; r += (gridDim.x * blockDim.x) >> 5) {
         const int t = __ldg(gather + r) / k;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
-        uint4 *dst = reinterpret_cast<uint4 *>(pool + (size_t)r * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(pool + (size_t)r * pool_pitch);
         for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
     }
 }
@@ -152,10 +152,11 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *offset_E, int k,
-                        int H, int rows_bound, uint8_t *pool, cudaStream_t s) {
+                        int H, int rows_bound, uint8_t *pool, int pool_pitch, cudaStream_t s) {
     const int warps = 8;
     const int blocks = max(1, min((rows_bound + warps - 1) / warps, 65535));
-    pool_gather_kernel<<<blocks, warps * 32, 0, s>>>(x, gather, offset_E, k, H, rows_bound, pool);
+    pool_gather_kernel<<<blocks, warps * 32, 0, s>>>(x, gather, offset_E, k, H, rows_bound, pool,
+                                                      pool_pitch);
 }
 
 void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }
             // this warp's 64 outputs are intermediate columns [64 jb, 64 jb + 64)
-            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.I + jb * 64);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + jb * 64);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
                 dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);

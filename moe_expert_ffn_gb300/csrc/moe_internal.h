@@ -41,10 +41,10 @@ struct L1Params {
     const float *x_sf;        // [T, H/128]
     const float *topk_w;      // [T*k]
     const float2 *w1_sf;      // [E, 2I/128, H/128] (gate scale, up scale) per interleaved block
-    uint8_t *l2_acts;         // [Pmax, I]
+    uint8_t *l2_acts;         // [Pmax, I], row pitch acts_pitch bytes
     float *l2_sf;             // [I/64, Pmax]
     int *err;
-    int H, I, E, k, Pmax;
+    int H, I, E, k, Pmax, acts_pitch;
     float clamp;
 };
 // gather_a: tm_a maps x [T, H] with one-row boxes (rows gathered in the
@@ -55,7 +55,7 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, i
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
 // first offset[E] rows (rows_bound = T*k is the host-side upper bound).
 void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *offset_E, int k,
-                        int H, int rows_bound, uint8_t *pool, cudaStream_t s);
+                        int H, int rows_bound, uint8_t *pool, int pool_pitch, cudaStream_t s);
 
 // L2: l2_acts . W2^T with per-64 activation scales, BF16 out in pool order.
 struct L2Params {
@@ -76,11 +76,11 @@ struct Fp4Params {
     const uint8_t *a_sf;      // L1: x scales u8 [T, H/32]; L2: l2 act scales u8 [Pmax, I/32]
     const uint8_t *b_sf;      // L1: W1 scales u8 [E*2I, H/32] (interleaved rows); L2: u8 [E*H, I/32]
     const float *topk_w;      // [T*k] (L1)
-    uint8_t *l2_acts;         // [Pmax, I] (L1 output)
+    uint8_t *l2_acts;         // [Pmax, I] (L1 output), row pitch acts_pitch bytes
     uint8_t *l2_sf;           // u8 [Pmax, I/32] (L1 output)
     uint16_t *l2_out;         // bf16 [Pmax, H] (L2 output)
     int *err;
-    int H, I, E, k, Pmax;
+    int H, I, E, k, Pmax, acts_pitch;
     float clamp;
 };
 void launch_fp4_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
@@ -91,15 +91,15 @@ void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const Fp4Params 
 // FP4 weight transform: W1 packed rows and their UE8M0 scale rows interleaved
 // like the FP8 rows (row bytes given), W2 copied by the caller.
 void launch_interleave_rows(const uint8_t *src, uint8_t *dst, int E, int I, int row_bytes,
-                            cudaStream_t s);
+                            int dst_pitch, cudaStream_t s);
 
 // Combine: y[t] = bf16( sum_j bf16 l2_out[pair_pool[t*k+j]] ) in slot order.
 void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int k, int H,
                     uint16_t *y, cudaStream_t s);
 
 // Weight transform (W1 gate/up interleave in groups of 8 rows, scale pairs).
-void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, float2 *w1i_sf,
-                         int E, int H, int I, cudaStream_t s);
+void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, int w1i_pitch,
+                         float2 *w1i_sf, int E, int H, int I, cudaStream_t s);
 
 size_t l1_smem_bytes();
 size_t l2_smem_bytes();

@@ -17,9 +17,10 @@
 namespace moe {
 namespace {
 
-// Rows of [E, 2I, row_bytes] in the interleaved order; row_bytes % 4 == 0.
+// Rows of [E, 2I, row_bytes] in the interleaved order, written with a row
+// pitch of dst_pitch bytes; row_bytes and dst_pitch multiples of 4.
 __global__ void interleave_rows_kernel(const uint8_t *__restrict__ src_rows, uint8_t *__restrict__ dst_rows,
-                                       int rows_total, int row_bytes, int I) {
+                                       int rows_total, int row_bytes, int dst_pitch, int I) {
     const int words = row_bytes / 4;
     for (int row = blockIdx.x; row < rows_total; row += gridDim.x) {
         const int e = row / (2 * I);
@@ -27,7 +28,7 @@ __global__ void interleave_rows_kernel(const uint8_t *__restrict__ src_rows, uin
         const int g = r >> 4, m = r & 15;
         const int src = (m < 8) ? (8 * g + m) : (I + 8 * g + m - 8);
         const uint32_t *s = reinterpret_cast<const uint32_t *>(src_rows + ((size_t)e * 2 * I + src) * row_bytes);
-        uint32_t *d = reinterpret_cast<uint32_t *>(dst_rows + (size_t)row * row_bytes);
+        uint32_t *d = reinterpret_cast<uint32_t *>(dst_rows + (size_t)row * dst_pitch);
         for (int v = threadIdx.x; v < words; v += blockDim.x) d[v] = s[v];
     }
 }
@@ -48,18 +49,18 @@ __global__ void interleave_w1_sf_kernel(const float *__restrict__ sf, float2 *__
 
 }  // namespace
 
-void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, float2 *w1i_sf, int E,
-                         int H, int I, cudaStream_t s) {
+void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, int w1i_pitch,
+                         float2 *w1i_sf, int E, int H, int I, cudaStream_t s) {
     const int rows = E * 2 * I;
-    interleave_rows_kernel<<<min(rows, 65535), 256, 0, s>>>(w1, w1i, rows, H, I);
+    interleave_rows_kernel<<<min(rows, 65535), 256, 0, s>>>(w1, w1i, rows, H, w1i_pitch, I);
     const int n = E * (2 * I / 128) * (H / 128);
     interleave_w1_sf_kernel<<<min((n + 255) / 256, 4096), 256, 0, s>>>(w1_sf, w1i_sf, E, H, I);
 }
 
 void launch_interleave_rows(const uint8_t *src, uint8_t *dst, int E, int I, int row_bytes,
-                            cudaStream_t s) {
+                            int dst_pitch, cudaStream_t s) {
     const int rows = E * 2 * I;
-    interleave_rows_kernel<<<min(rows, 65535), 128, 0, s>>>(src, dst, rows, row_bytes, I);
+    interleave_rows_kernel<<<min(rows, 65535), 128, 0, s>>>(src, dst, rows, row_bytes, dst_pitch, I);
 }
 
 }  // namespace moe
