@@ -202,7 +202,7 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128, packed) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128, packed)
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
-                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128));
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256));
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
              make_map(&c->tm_pool.box[i], c->ws + L.pool, H, Pm, L.pool_pitch, 128, 32u << i);

@@ -27,10 +27,10 @@
 //              product (the pages' "promotion"); after the last block,
 //              SwiGLU/requantise (L1) or BF16 (L2) and store.
 // L1: 128 x 256 tiles (128 gate/up pairs = two 64-column output groups), two
-// 256-column accumulators.  L2: 128 x 128 tiles, a ring of four 128-column
-// accumulators (one per 64-K half).  Register budget: 168 per thread; the
-// epilogue keeps 128 (L1) or 64 (L2) accumulators and loads TMEM in small
-// pieces so nothing spills.
+// 256-column accumulators, one per 128-K block.  L2: 128 x 256 tiles, two
+// 256-column accumulators, one per 64-K half.  Register budget: 168 per
+// thread; each epilogue thread keeps 128 accumulators and loads TMEM in
+// 16-column pieces so nothing spills.
 #include "moe_device.cuh"
 #include "moe_gemm_common.cuh"
 #include "moe_internal.h"
@@ -52,10 +52,12 @@ constexpr int kL1Stages = 4;
 constexpr uint32_t kL1ABytes = kBM * kBK;
 constexpr uint32_t kL1BBytes = kL1BN * kBK;
 constexpr uint32_t kL1StageBytes = kL1ABytes + kL1BBytes;
-// L2: 128 x 128 tiles, four 128-column accumulators, 6 stages of 32 KB
-constexpr int kL2BN = 128;
-constexpr int kL2TBufs = 4;
-constexpr int kL2Stages = 6;
+// L2: 128 x 256 tiles, a ring of two 256-column accumulators (one per 64-K
+// half of a stage), 4 stages of 48 KB.  (A K=32 MMA takes about the same
+// time at N=128 as at N=256, so the wide tile doubles the tensor throughput.)
+constexpr int kL2BN = 256;
+constexpr int kL2TBufs = 2;
+constexpr int kL2Stages = 4;
 constexpr uint32_t kL2ABytes = kBM * kBK;
 constexpr uint32_t kL2BBytes = kL2BN * kBK;
 constexpr uint32_t kL2StageBytes = kL2ABytes + kL2BBytes;
@@ -121,7 +123,7 @@ __device__ __forceinline__ void drain_producer(Ctrl *ctrl, int it, int stages) {
         drain_wait(smem_u32(&ctrl->full[i % stages]), (i / stages) & 1);
 }
 
-// L1: promote this warp's 128 columns (TMEM columns tcol..tcol+127 of the
+// Promote this warp's 128 columns (TMEM columns tcol..tcol+127 of the
 // thread's lane) into acc[128] in 16-column pieces, and release the buffer
 // as soon as the last piece has landed.  Gate columns are 0-7 of every 16,
 // up columns 8-15: each piece has 8 of each.
@@ -137,21 +139,6 @@ __device__ __forceinline__ void promote_l1(float (&acc)[128], uint32_t tcol, flo
         for (int i = 0; i < 8; ++i) acc[16 * c + i] = fmaf(v[i], s_gate, acc[16 * c + i]);
 #pragma unroll
         for (int i = 8; i < 16; ++i) acc[16 * c + i] = fmaf(v[i], s_up, acc[16 * c + i]);
-    }
-}
-
-// L2: promote this warp's 64 columns into acc[64], one scale for all.
-__device__ __forceinline__ void promote_l2(float (&acc)[64], uint32_t tcol, float sc, Ctrl *ctrl,
-                                           int b, uint32_t lane) {
-    float v0[32], v1[32];
-    tmem_ld32(tcol, v0);
-    tmem_ld32(tcol + 32, v1);
-    tmem_ld_wait();
-    release_tbuf(ctrl, b, lane);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        acc[i] = fmaf(v0[i], sc, acc[i]);
-        acc[32 + i] = fmaf(v1[i], sc, acc[32 + i]);
     }
 }
 
@@ -366,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
-    const int NB = p.H / kL2BN;
+    const int NB = (p.H + kL2BN - 1) / kL2BN;   // the last block may be half empty (H % 256 == 128)
     const int KB = p.I / kBK;
     const int total = __ldg(p.mb_prefix + p.E) * NB;
 
@@ -446,59 +433,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             drain_wait(smem_u32(&ctrl->tfull[(kt - 1) % kL2TBufs]), ((kt - 1) / kL2TBufs) & 1);
     } else {
         const int q = warp & 3;
-        const int h = (warp - kEpiWarp0) >> 2;   // which 64 of the 128 tile columns
+        const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = q * 32 + (int)lane;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 64;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const size_t ps = (size_t)p.Pmax;
+        const int HB = p.H / 128;                // 128-row weight scale blocks
         int kt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
-            const bool valid = lrow < t.rows;
-            const bool warp_on = q * 32 < t.rows;
+            const int cb = t.nb * 2 + h;         // this warp's 128-column block of H
+            const bool cols_ok = cb < HB;
+            const bool valid = lrow < t.rows && cols_ok;
+            const bool warp_on = q * 32 < t.rows && cols_ok;
             const int row = t.row0 + lrow;
-            const float *sfb = p.w2_sf + ((size_t)t.e * NB + t.nb) * KB;
+            const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
             const float *sfa = p.l2_sf + row;   // 64-K half j of the K loop: sfa[j * Pmax]
 
-            float acc[64];
+            float acc[128];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
-            // one 128-K block (two halves, two ring buffers) per iteration;
-            // scales prefetched one block ahead
-            float sa0_n = valid ? __ldg(sfa) : 0.0f;
-            float sa1_n = valid ? __ldg(sfa + ps) : 0.0f;
-            float sb_n = __ldg(sfb);
-            for (int kb = 0; kb < KB; ++kb, kt += 2) {
-                const float s0 = sa0_n * sb_n, s1 = sa1_n * sb_n;
-                if (kb + 1 < KB) {
-                    if (valid) {
-                        sa0_n = __ldg(sfa + (size_t)(2 * kb + 2) * ps);
-                        sa1_n = __ldg(sfa + (size_t)(2 * kb + 3) * ps);
-                    }
-                    sb_n = __ldg(sfb + kb + 1);
+            // scales of half j+1 prefetched while half j is promoted
+            float sa_n = valid ? __ldg(sfa) : 0.0f;
+            float sb = __ldg(sfb);
+            for (int j = 0; j < 2 * KB; ++j, ++kt) {
+                const float sc = sa_n * sb;
+                if (j + 1 < 2 * KB) {
+                    if (valid) sa_n = __ldg(sfa + (size_t)(j + 1) * ps);
+                    if (j & 1) sb = __ldg(sfb + ((j + 1) >> 1));
                 }
-                const int b0 = kt % kL2TBufs, b1 = (kt + 1) % kL2TBufs;
-                if (!mbar_wait(smem_u32(&ctrl->tfull[b0]), (kt / kL2TBufs) & 1, abort_flag, p.err) ||
-                    !mbar_wait(smem_u32(&ctrl->tfull[b1]), ((kt + 1) / kL2TBufs) & 1, abort_flag,
-                               p.err)) {
+                const int b = kt % kL2TBufs;
+                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (kt / kL2TBufs) & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (warp_on) {
-                    promote_l2(acc, t_lane + b0 * kL2BN, s0, ctrl, b0, lane);
-                    promote_l2(acc, t_lane + b1 * kL2BN, s1, ctrl, b1, lane);
-                } else {
-                    release_tbuf(ctrl, b0, lane);
-                    release_tbuf(ctrl, b1, lane);
-                }
+                if (warp_on)
+                    promote_l1(acc, t_lane + b * kL2BN, sc, sc, ctrl, b, lane);
+                else
+                    release_tbuf(ctrl, b, lane);
             }
             if (!ok || !valid) continue;
-            uint4 *dst =
-                reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + t.nb * kL2BN + h * 64);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + cb * 128);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
+            for (int v = 0; v < 16; ++v)
                 dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]), bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
                                     bf16x2(acc[8 * v + 4], acc[8 * v + 5]), bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
         }
