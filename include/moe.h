@@ -141,7 +141,7 @@ MOE_API int moe_get_dispatch(moe_ctx *ctx, int32_t *counts, int32_t *offsets, in
 
 /* Copy intermediates of the last forward (T tokens; row r belongs to pair
  * gather[r], rows r >= offsets[E] unspecified), P = T*k:
- * l2_acts u8 (E4M3) [P, I], l2_sf = the L2 activation scales (f32 [I/64, P]
+ * l2_acts u8 (E4M3) [P, I], l2_sf = the L2 activation scales (f32 [P, I/64]
  * with FP8 weights, u8 UE8M0 [P, I/32] with FP4 weights),
  * l2_out bf16 [P, H] (the rounded L2 outputs).  Any pointer may be NULL.
  * For stage-by-stage tests. */

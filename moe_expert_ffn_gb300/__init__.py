@@ -227,7 +227,7 @@ class MoELayer:
         if self.fp4:
             sf = torch.empty(P, self.I // 32, dtype=torch.uint8, device=self.device)
         else:
-            sf = torch.empty(self.I // 64, P, dtype=torch.float32, device=self.device)
+            sf = torch.empty(P, self.I // 64, dtype=torch.float32, device=self.device)
         out = torch.empty(P, self.H, dtype=torch.bfloat16, device=self.device)
         _check(lib().moe_get_intermediates(self._ctx, _ptr(acts), _ptr(sf), _ptr(out), _stream(stream)),
                "moe_get_intermediates")

@@ -433,8 +433,7 @@ int moe_get_intermediates(moe_ctx *c, void *l2_acts, void *l2_sf, void *l2_out, 
     if (l2_sf) {
         const cudaError_t e =
             c->cfg.wfmt == MOE_W_FP8_BLK128
-                ? cudaMemcpy2DAsync(l2_sf, P * 4, c->ws + c->L.l2_sf, Pm * 4, P * 4, I / 64,
-                                    cudaMemcpyDeviceToDevice, s)
+                ? cudaMemcpyAsync(l2_sf, c->ws + c->L.l2_sf, P * (I / 64) * 4, cudaMemcpyDeviceToDevice, s)
                 : cudaMemcpyAsync(l2_sf, c->ws + c->L.l2_sf, P * (I / 32), cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }

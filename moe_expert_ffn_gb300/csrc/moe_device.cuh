@@ -62,6 +62,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or `ns` nanoseconds pass, so a waiting warp takes no issue
+// slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kWaitSleepNs = 100000;   // abort flag and clock checked every 100 us
+
 // Wait for the phase with the given parity to complete.  Gives up when the
 // CTA's abort flag is raised or after kWaitTimeoutNs; on a timeout it raises
 // the abort flag and records kErrTimeout in the device error word.  Returns
@@ -71,9 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
             *abort_flag = 1;

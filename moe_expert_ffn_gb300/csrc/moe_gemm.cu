@@ -38,9 +38,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kNumEpiWarps = 8;
-constexpr int kEpiWarp0 = 2;                 // warps 2..9 run the epilogue
+constexpr int kEpiWarp0 = 2;                 // warps 2.. run the epilogue
+constexpr int kL1EpiWarps = 8;               // L1: two warps per TMEM lane quadrant
+constexpr int kL1Threads = 32 * (kEpiWarp0 + kL1EpiWarps);
+constexpr int kL2EpiWarps = 8;               // L2: two warps per TMEM lane quadrant
+constexpr int kL2Threads = 32 * (kEpiWarp0 + kL2EpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStages = 6;
 constexpr int kMaxTBufs = 4;
@@ -78,7 +80,8 @@ constexpr size_t kL1SmemBytes = 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrl
 constexpr size_t kL2SmemBytes = 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes;
 
 // Common prologue: barriers, TMEM allocation.  Returns the TMEM base.
-__device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages, int tbufs) {
+__device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages, int tbufs,
+                                               int epi_warps) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
@@ -86,7 +89,7 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages,
         }
         for (int b = 0; b < tbufs; ++b) {
             mbar_init(smem_u32(&ctrl->tfull[b]), 1);
-            mbar_init(smem_u32(&ctrl->tempty[b]), kNumEpiWarps);
+            mbar_init(smem_u32(&ctrl->tempty[b]), epi_warps);
         }
         ctrl->abort = 0;
         fence_mbar_init();
@@ -124,11 +127,14 @@ __device__ __forceinline__ void drain_producer(Ctrl *ctrl, int it, int stages) {
 }
 
 // Promote this warp's 128 columns (TMEM columns tcol..tcol+127 of the
-// thread's lane) into acc[128] in 16-column pieces, and release the buffer
-// as soon as the last piece has landed.  Gate columns are 0-7 of every 16,
-// up columns 8-15: each piece has 8 of each.
-__device__ __forceinline__ void promote_l1(float (&acc)[128], uint32_t tcol, float s_gate,
-                                           float s_up, Ctrl *ctrl, int b, uint32_t lane) {
+// thread's lane) into 128 FP32 accumulators, held as 64 pairs (acc[i] =
+// columns 2i, 2i+1), in 16-column pieces, and release the buffer as soon as
+// the last piece has landed.  Columns 0-7 of every 16 take s_lo, columns 8-15
+// s_hi (L1: gate and up scales; L2: one scale).  Packed FP32 FMAs: each half
+// is an IEEE fma rounded to nearest, the same result as fmaf.
+__device__ __forceinline__ void promote128(float2 (&acc)[64], uint32_t tcol, float s_lo, float s_hi,
+                                           Ctrl *ctrl, int b, uint32_t lane) {
+    const float2 sl = make_float2(s_lo, s_lo), sh = make_float2(s_hi, s_hi);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         float v[16];
@@ -136,10 +142,16 @@ __device__ __forceinline__ void promote_l1(float (&acc)[128], uint32_t tcol, flo
         tmem_ld_wait();
         if (c == 7) release_tbuf(ctrl, b, lane);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[16 * c + i] = fmaf(v[i], s_gate, acc[16 * c + i]);
+        for (int i = 0; i < 4; ++i)
+            acc[8 * c + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), sl, acc[8 * c + i]);
 #pragma unroll
-        for (int i = 8; i < 16; ++i) acc[16 * c + i] = fmaf(v[i], s_up, acc[16 * c + i]);
+        for (int i = 4; i < 8; ++i)
+            acc[8 * c + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), sh, acc[8 * c + i]);
     }
+}
+
+__device__ __forceinline__ float acc_at(const float2 (&acc)[64], int i) {
+    return (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
 }
 
 // ============================================================================
@@ -149,7 +161,7 @@ __device__ __forceinline__ void promote_l1(float (&acc)[128], uint32_t tcol, flo
 // boxes one row high); otherwise A is the pool of gathered rows written by
 // the dispatch step (tm_a = pool, 128-row boxes).
 template <bool kFast, bool kGatherA>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kL1Threads, 1)
     l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
               const L1Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_w1);
     }
-    const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs);
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs, kL1EpiWarps);
     volatile int *abort_flag = &ctrl->abort;
 
     if (warp == 0) {
@@ -269,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
             const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
 
-            float acc[128];
+            float2 acc[64];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
             // scale factors prefetched one K block ahead
             float sa_n = valid ? __ldg(sfa) : 0.0f;
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (warp_on)
-                    promote_l1(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
+                    promote128(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
                 else
                     release_tbuf(ctrl, b, lane);
             }
@@ -301,18 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float wgt = __ldg(p.topk_w + pair);
             const float clampv = p.clamp;
             float amax = 0.0f;
+            float act[64];
 #pragma unroll
             for (int o = 0; o < 64; ++o) {
                 const int gi = 16 * (o >> 3) + (o & 7);
-                const float g = fminf(fmaxf(acc[gi], -clampv), clampv);
-                const float u = fminf(fmaxf(acc[gi + 8], -clampv), clampv);
+                const float g = fminf(fmaxf(acc_at(acc, gi), -clampv), clampv);
+                const float u = fminf(fmaxf(acc_at(acc, gi + 8), -clampv), clampv);
                 float silu;
                 if (kFast)
                     silu = __fdividef(g, 1.0f + __expf(-g));
                 else
                     silu = g / (1.0f + expf(-g));
                 const float a = silu * u * wgt;
-                acc[gi] = a;
+                act[o] = a;
                 amax = fmaxf(amax, fabsf(a));
             }
             // per-64 FP8 requantisation: sf = amax / 448, q = e4m3(a / sf)
@@ -324,8 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int o = w4 * 4 + j;
-                    const float a = acc[16 * (o >> 3) + (o & 7)];
-                    qv[j] = (sf == 0.0f) ? 0.0f : __fdiv_rn(a, sf);
+                    qv[j] = (sf == 0.0f) ? 0.0f : __fdiv_rn(act[o], sf);
                 }
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int v = 0; v < 4; ++v)
                 dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            p.l2_sf[(size_t)jb * p.Pmax + row] = sf;
+            p.l2_sf[(size_t)row * (p.I / 64) + jb] = sf;
         }
     }
     gemm_teardown(tmem, warp);
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 // L2: down GEMM with per-64 activation scales, BF16 output in pool order
 // ============================================================================
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kL2Threads, 1)
     l2_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w2,
               const L2Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_w2);
     }
-    const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs);
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
     volatile int *abort_flag = &ctrl->abort;
 
     if (warp == 0) {
@@ -436,7 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = q * 32 + (int)lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-        const size_t ps = (size_t)p.Pmax;
         const int HB = p.H / 128;                // 128-row weight scale blocks
         int kt = 0;
         bool ok = true;
@@ -448,38 +459,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_on = q * 32 < t.rows && cols_ok;
             const int row = t.row0 + lrow;
             const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
-            const float *sfa = p.l2_sf + row;   // 64-K half j of the K loop: sfa[j * Pmax]
+            // the row's two 64-K activation scales of 128-K block kb: sfa[kb]
+            const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)row * (p.I / 64));
 
-            float acc[128];
+            float2 acc[64];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-            // scales of half j+1 prefetched while half j is promoted
-            float sa_n = valid ? __ldg(sfa) : 0.0f;
-            float sb = __ldg(sfb);
-            for (int j = 0; j < 2 * KB; ++j, ++kt) {
-                const float sc = sa_n * sb;
-                if (j + 1 < 2 * KB) {
-                    if (valid) sa_n = __ldg(sfa + (size_t)(j + 1) * ps);
-                    if (j & 1) sb = __ldg(sfb + ((j + 1) >> 1));
+            // scales prefetched two 128-K blocks ahead (a far L2 hit takes
+            // longer than one block's promotion)
+            const float2 z2 = make_float2(0.0f, 0.0f);
+            float2 sa0 = valid ? __ldg(sfa) : z2;
+            float2 sa1 = (valid && KB > 1) ? __ldg(sfa + 1) : z2;
+            float sb0 = __ldg(sfb);
+            float sb1 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
+            for (int kb = 0; ok && kb < KB; ++kb) {
+                const float2 sa = sa0;
+                const float sb = sb0;
+                sa0 = sa1;
+                sb0 = sb1;
+                if (kb + 2 < KB) {
+                    if (valid) sa1 = __ldg(sfa + kb + 2);
+                    sb1 = __ldg(sfb + kb + 2);
                 }
-                const int b = kt % kL2TBufs;
-                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (kt / kL2TBufs) & 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
+#pragma unroll
+                for (int half = 0; half < 2; ++half, ++kt) {
+                    const float sc = (half ? sa.y : sa.x) * sb;
+                    const int b = kt % kL2TBufs;
+                    if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (kt / kL2TBufs) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (warp_on)
+                        promote128(acc, t_lane + b * kL2BN, sc, sc, ctrl, b, lane);
+                    else
+                        release_tbuf(ctrl, b, lane);
                 }
-                tc_fence_after();
-                if (warp_on)
-                    promote_l1(acc, t_lane + b * kL2BN, sc, sc, ctrl, b, lane);
-                else
-                    release_tbuf(ctrl, b, lane);
             }
             if (!ok || !valid) continue;
             uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + cb * 128);
 #pragma unroll
             for (int v = 0; v < 16; ++v)
-                dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]), bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                                    bf16x2(acc[8 * v + 4], acc[8 * v + 5]), bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+                dst[v] = make_uint4(bf16x2(acc[4 * v].x, acc[4 * v].y), bf16x2(acc[4 * v + 1].x, acc[4 * v + 1].y),
+                                    bf16x2(acc[4 * v + 2].x, acc[4 * v + 2].y),
+                                    bf16x2(acc[4 * v + 3].x, acc[4 * v + 3].y));
         }
     }
     gemm_teardown(tmem, warp);
@@ -499,7 +523,7 @@ static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Par
                              (int)kL1SmemBytes);
         configured = true;
     }
-    l1_kernel<kFast, kGatherA><<<num_sms, kThreads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
+    l1_kernel<kFast, kGatherA><<<num_sms, kL1Threads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
 }
 
 void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
@@ -520,7 +544,7 @@ void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p, i
         cudaFuncSetAttribute(l2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
         configured = true;
     }
-    l2_kernel<<<num_sms, kThreads, kL2SmemBytes, s>>>(tm_a, tm_w2, p);
+    l2_kernel<<<num_sms, kL2Threads, kL2SmemBytes, s>>>(tm_a, tm_w2, p);
 }
 
 }  // namespace moe

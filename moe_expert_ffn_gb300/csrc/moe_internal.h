@@ -42,7 +42,7 @@ struct L1Params {
     const float *topk_w;      // [T*k]
     const float2 *w1_sf;      // [E, 2I/128, H/128] (gate scale, up scale) per interleaved block
     uint8_t *l2_acts;         // [Pmax, I], row pitch acts_pitch bytes
-    float *l2_sf;             // [I/64, Pmax]
+    float *l2_sf;             // [Pmax, I/64]
     int *err;
     int H, I, E, k, Pmax, acts_pitch;
     float clamp;
@@ -60,7 +60,7 @@ void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *
 // L2: l2_acts . W2^T with per-64 activation scales, BF16 out in pool order.
 struct L2Params {
     const int32_t *offset, *mb_prefix, *mblk_expert;
-    const float *l2_sf;       // [I/64, Pmax]
+    const float *l2_sf;       // [Pmax, I/64]
     const float *w2_sf;       // [E, H/128, I/128]
     uint16_t *l2_out;         // [Pmax, H] bf16
     int *err;

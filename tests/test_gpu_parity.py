@@ -79,7 +79,7 @@ def test_l2_activations_stage_by_stage(m, orc):
         pair = int(gather[r])
         t, j = divmod(pair, wl.k)
         pr = orc.pair(inp, t, int(idx[t, j]), float(w[t, j]))
-        np.testing.assert_allclose(sf[:, r], pr["sf"], rtol=1e-5, atol=0)
+        np.testing.assert_allclose(sf[r], pr["sf"], rtol=1e-5, atol=0)
         code_mismatch += int((acts[r] != pr["q"]).sum())
         total += wl.I
         ob = bf16_bits_to_float(pr["ob"])
