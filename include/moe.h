@@ -82,7 +82,8 @@ typedef struct {
     int wfmt;         /* moe_wfmt */
     float act_clamp;  /* symmetric clamp of gate and up before SwiGLU; +INFINITY = off
                          (design §10.1 step 3, §1.1 decision 16) */
-    int fast_math;    /* 0: expf and IEEE division in SwiGLU; 1: __expf / fast divide */
+    int fast_math;    /* SwiGLU exponential: 0 expf (accurate), 1 __expf; the
+                         division is the fast one (<= 2 ulp) either way */
 } moe_config;
 
 /* Bytes of device workspace / transformed-weight storage for `cfg`

@@ -26,7 +26,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
     size_t pool_pitch, acts_pitch, w1_pitch, w2_pitch;   // bytes per row
     // workspace
-    size_t err, count, offset, mb_prefix, mblk_expert, gather, pair_pool;
+    size_t err, count, offset, mb_prefix, mblk_expert, mb2_prefix, mblk2_expert, gather, pair_pool;
     size_t pool, l2_acts, l2_sf, l2_out;
     size_t st_x, st_xsf, st_idx, st_w, st_y;
     size_t ws_total;
@@ -72,6 +72,8 @@ Layout make_layout(const moe_config *c) {
     L.offset = take(4 * (E + 1), 256);
     L.mb_prefix = take(4 * (E + 1), 256);
     L.mblk_expert = take(4 * MBmax, 256);
+    L.mb2_prefix = take(4 * (E + 1), 256);
+    L.mblk2_expert = take(4 * (Pm / (2 * kBM) + E + 1), 256);
     L.gather = take(4 * Pm, 256);
     L.pair_pool = take(4 * Pm, 256);
     L.pool = take(Pm * L.pool_pitch, kAlign);
@@ -156,8 +158,10 @@ struct moe_ctx {
     bool weights_ready;
     int last_T;
     CUtensorMap tm_w1, tm_w2;
+    CUtensorMap tm_w1h;     // FP8 W1i with 128-row boxes (CTA-pair L1)
     AMaps tm_l2a, tm_pool;
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
+    int l1_pair_mode;       // 0 auto, 1 CTA pairs, 2 single CTAs
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
     int prof_max, prof_n;
 
@@ -202,6 +206,7 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128, packed) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128, packed)
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
+                         make_map(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256));
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
@@ -216,6 +221,9 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
         if (!strcmp(m, "gather")) c->l1_a_mode = 1;
         if (!strcmp(m, "pool")) c->l1_a_mode = 2;
     }
+    // L1 on CTA pairs: MOE_L1_PAIR=1|0 overrides the automatic choice
+    c->l1_pair_mode = 0;
+    if (const char *m = getenv("MOE_L1_PAIR")) c->l1_pair_mode = (m[0] == '1') ? 1 : 2;
     // zero the error word
     if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * 4) != cudaSuccess) {
         free(c);
@@ -284,6 +292,8 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     o.offset = c->w<int32_t>(L.offset);
     o.mb_prefix = c->w<int32_t>(L.mb_prefix);
     o.mblk_expert = c->w<int32_t>(L.mblk_expert);
+    o.mb2_prefix = c->w<int32_t>(L.mb2_prefix);
+    o.mblk2_expert = c->w<int32_t>(L.mblk2_expert);
     o.gather = c->w<int32_t>(L.gather);
     o.pair_pool = c->w<int32_t>(L.pair_pool);
     o.stats = stats;
@@ -343,6 +353,8 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     p1.offset = o.offset;
     p1.mb_prefix = o.mb_prefix;
     p1.mblk_expert = o.mblk_expert;
+    p1.mb2_prefix = o.mb2_prefix;
+    p1.mblk2_expert = o.mblk2_expert;
     p1.x_sf = static_cast<const float *>(x_sf);
     p1.topk_w = topk_weights;
     p1.w1_sf = c->wt_at<float2>(L.w1i_sf);
@@ -356,7 +368,16 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
     p1.k = k;
     p1.Pmax = Pm;
     p1.clamp = g.act_clamp;
-    launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
+    // CTA pairs only on request for now (MOE_L1_PAIR=1): single CTAs are
+    // faster end to end on every measured workload
+    const bool pair = c->l1_pair_mode == 1;
+    if (pair) {
+        if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_w1h, p1, g.fast_math, gather_a, c->num_sms, s) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else {
+        launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
+    }
     if (ev) cudaEventRecord(ev[2], s);
 
     L2Params p2;

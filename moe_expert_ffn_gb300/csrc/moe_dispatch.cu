@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *hist = sm;                 // [kWarps][E]: count, then first slot of the warp
     int32_t *off_s = sm + kWarps * E;   // [E+1]
     __shared__ int warp_tot[kWarps];
-    __shared__ int tot_a, tot_b, bad;
+    __shared__ int tot_a, tot_b, tot_c, bad;
 
     const int P = T * k;
     const int warp = threadIdx.x >> 5;
@@ -92,8 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // E <= kThreads: one expert per thread for both prefix scans
     const int nmb = (cnt + kBM - 1) / kBM;
+    const int nmb2 = (cnt + 2 * kBM - 1) / (2 * kBM);
     const int off = block_exclusive_scan(cnt, warp_tot, &tot_a);
     const int mbo = block_exclusive_scan(nmb, warp_tot, &tot_b);
+    const int mbo2 = block_exclusive_scan(nmb2, warp_tot, &tot_c);
     if (threadIdx.x < E) {
         off_s[threadIdx.x] = off;
         o.count[threadIdx.x] = cnt;
@@ -101,11 +103,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         o.mb_prefix[threadIdx.x] = mbo;
         if (o.stats) o.stats[threadIdx.x] += cnt;
         for (int b = 0; b < nmb; ++b) o.mblk_expert[mbo + b] = threadIdx.x;
+        if (o.mb2_prefix) {
+            o.mb2_prefix[threadIdx.x] = mbo2;
+            for (int b = 0; b < nmb2; ++b) o.mblk2_expert[mbo2 + b] = threadIdx.x;
+        }
     }
     if (threadIdx.x == 0) {
         off_s[E] = tot_a;
         o.offset[E] = tot_a;
         o.mb_prefix[E] = tot_b;
+        if (o.mb2_prefix) o.mb2_prefix[E] = tot_c;
         if (bad) atomicOr(o.err, kErrBadExpert);
     }
     __syncthreads();
@@ -229,6 +236,8 @@ extern "C" MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tok
     o.pair_pool = scratch + kNaPairPool;
     o.mb_prefix = scratch + kNaMbPrefix;
     o.mblk_expert = scratch + kNaMblk;
+    o.mb2_prefix = nullptr;
+    o.mblk2_expert = nullptr;
     o.stats = nullptr;
     o.err = scratch + kNaErr;
     // the error word is only ever OR-ed into: start it at zero

@@ -323,13 +323,17 @@ __global__ void __launch_bounds__(kL1Threads, 1)
                 if (kFast)
                     silu = __fdividef(g, 1.0f + __expf(-g));
                 else
-                    silu = g / (1.0f + expf(-g));
+                    silu = __fdividef(g, 1.0f + expf(-g));
                 const float a = silu * u * wgt;
                 act[o] = a;
                 amax = fmaxf(amax, fabsf(a));
             }
             // per-64 FP8 requantisation: sf = amax / 448, q = e4m3(a / sf)
+            // q = e4m3(a / sf) as a times the correctly rounded 1/sf: within
+            // one f32 ulp of the quotient, so an E4M3 code can differ only
+            // for a quotient within an ulp of a rounding midpoint
             const float sf = amax / 448.0f;
+            const float rsf = (sf == 0.0f) ? 0.0f : __frcp_rn(sf);
             uint32_t pk[16];
 #pragma unroll
             for (int w4 = 0; w4 < 16; ++w4) {
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int o = w4 * 4 + j;
-                    qv[j] = (sf == 0.0f) ? 0.0f : __fdiv_rn(act[o], sf);
+                    qv[j] = (sf == 0.0f) ? 0.0f : act[o] * rsf;
                 }
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }

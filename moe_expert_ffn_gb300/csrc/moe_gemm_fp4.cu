@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kFast)
                         silu = __fdividef(g, 1.0f + __expf(-g));
                     else
-                        silu = g / (1.0f + expf(-g));
+                        silu = __fdividef(g, 1.0f + expf(-g));
                     acc[gi] = silu * u * wgt;
                 }
                 // two 32-column groups, UE8M0 scale 2^ceil(log2(amax/448)) each
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int o = 32 * grp; o < 32 * grp + 32; ++o)
                         amax = fmaxf(amax, fabsf(acc[16 * (o >> 3) + (o & 7)]));
                     const int e = ue8m0_exponent(amax);
-                    const float sf = ldexpf(1.0f, e);
+                    // a / 2^e as a * 2^-e: both exact powers of two, the same rounding
+                    const float rsf = ldexpf(1.0f, -e);
                     codes |= static_cast<uint32_t>(e + 127) << (8 * grp);
 #pragma unroll
                     for (int w4 = 8 * grp; w4 < 8 * grp + 8; ++w4) {
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 4; ++j) {
                             const int o = w4 * 4 + j;
                             const float a = acc[16 * (o >> 3) + (o & 7)];
-                            qv[j] = (amax == 0.0f) ? 0.0f : __fdiv_rn(a, sf);
+                            qv[j] = (amax == 0.0f) ? 0.0f : a * rsf;
                         }
                         pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
                     }

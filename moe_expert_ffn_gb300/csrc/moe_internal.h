@@ -26,6 +26,8 @@ struct DispatchOut {
     int32_t *offset;       // [E+1]  exclusive prefix of count
     int32_t *mb_prefix;    // [E+1]  exclusive prefix of ceil(count/128)
     int32_t *mblk_expert;  // [max M blocks]  expert of each M block
+    int32_t *mb2_prefix;   // [E+1]  exclusive prefix of ceil(count/256), or null
+    int32_t *mblk2_expert; // [max pair blocks]  expert of each 256-row block
     int32_t *gather;       // [T*k]  pool row -> pair id t*k+j (stable order)
     int32_t *pair_pool;    // [T*k]  pair id -> pool row, -1 if inactive
     int32_t *stats;        // [E] or null: += count
@@ -38,6 +40,7 @@ void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const Dispatc
 // L1: x (gathered by pool row) . W1i^T, SwiGLU * w, per-64 FP8 requant.
 struct L1Params {
     const int32_t *gather, *offset, *mb_prefix, *mblk_expert;
+    const int32_t *mb2_prefix, *mblk2_expert;   // 256-row blocks (CTA-pair kernel)
     const float *x_sf;        // [T, H/128]
     const float *topk_w;      // [T*k]
     const float2 *w1_sf;      // [E, 2I/128, H/128] (gate scale, up scale) per interleaved block
@@ -51,6 +54,12 @@ struct L1Params {
 // kernel); otherwise tm_a maps the pool [Pmax, H] with 128-row boxes.
 void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
                bool gather_a, int num_sms, cudaStream_t s);
+
+// L1 on CTA pairs (moe_gemm_pair.cu): 256 x 256 tiles, one M=256 MMA over
+// both CTAs; tm_w1h maps W1i with 128-row boxes (each CTA stages half a tile).
+cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_w1h, const L1Params &p, int fast_math,
+                           bool gather_a, int num_sms, cudaStream_t s);
+size_t l1_pair_smem_bytes();
 
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
 // first offset[E] rows (rows_bound = T*k is the host-side upper bound).

@@ -88,6 +88,52 @@ def test_l2_activations_stage_by_stage(m, orc):
     assert code_mismatch <= 0.01 * total, (code_mismatch, total)
 
 
+def _crafted_counts(T, k, E, counts, seed):
+    """topk_idx [T, k] with distinct experts per token and the given per-expert counts."""
+    assert sum(counts) == T * k and len(counts) == E and max(counts) <= T
+    # experts sorted, slots filled column by column: a run of <= T equal ids
+    # never puts one expert in two slots of a token; then shuffle the tokens
+    ids = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])
+    idx = ids.reshape(k, T).T.copy()
+    np.random.default_rng(seed).shuffle(idx)
+    assert all(len(set(r)) == k for r in idx.tolist())
+    return torch.from_numpy(idx)
+
+
+# L1 on CTA pairs (256-row blocks): experts whose counts leave the second CTA
+# empty (<= 128), ragged in either half, exactly one or two blocks, several
+# blocks (N-major), plus the generic small cases
+PAIR_CASES = SMALL[1:3] + [moe_synth.custom(T=600, H=384, I=256, E=8, k=2, seed=37, name="pair_counts")]
+PAIR_COUNTS = {"pair_counts": [1, 127, 128, 129, 255, 256, 257, 47]}
+
+
+@pytest.mark.parametrize("a_mode", ["pool", "gather"])
+@pytest.mark.parametrize("wl", PAIR_CASES, ids=lambda w: w.name)
+def test_l1_cta_pairs_match_oracle(m, orc, wl, a_mode, monkeypatch):
+    monkeypatch.setenv("MOE_L1_PAIR", "1")
+    monkeypatch.setenv("MOE_L1_A", a_mode)
+    inp = moe_synth.make_inputs(wl)
+    if wl.name in PAIR_COUNTS:
+        inp["topk_idx"] = _crafted_counts(wl.T, wl.k, wl.E, PAIR_COUNTS[wl.name], wl.seed)
+    layer, g, y = _run(m, wl, inp)
+    ref = bf16_bits_to_float(orc.forward(inp))
+    rel, mx = assert_y_close(y, ref, f"{wl.name}/pairs/{a_mode}")
+    # the L1 output itself: scales and FP8 codes of sampled rows
+    _, offsets, gather = layer.get_dispatch(wl.T)
+    acts, sf, _ = layer.get_intermediates(wl.T)
+    acts, sf, gather = acts.cpu().numpy(), sf.cpu().numpy(), gather.cpu().numpy()
+    idx, w = inp["topk_idx"].numpy(), inp["topk_weights"].numpy()
+    mism = total = 0
+    for r in range(0, int(offsets[-1]), 11):
+        t, j = divmod(int(gather[r]), wl.k)
+        pr = orc.pair(inp, t, int(idx[t, j]), float(w[t, j]))
+        np.testing.assert_allclose(sf[r], pr["sf"], rtol=1e-5, atol=0)
+        mism += int((acts[r] != pr["q"]).sum())
+        total += wl.I
+    assert mism <= 0.01 * total, (mism, total)
+    print(f"{wl.name}/pairs/{a_mode}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
+
+
 def test_zero_tokens_and_inactive_slots(m, orc):
     wl = moe_synth.custom(T=40, H=256, I=128, E=8, k=3, seed=35)
     inp = moe_synth.make_inputs(wl)
