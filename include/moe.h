@@ -190,6 +190,18 @@ MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tokens, int to
 MOE_API int moe_profile_begin(moe_ctx *ctx, int max_forwards);
 MOE_API int moe_profile_end(moe_ctx *ctx, float *stage_ms, int *n_forwards);
 
+/* Test of the device-side timeout path (the pages have no counterpart; it
+ * exists so that failure detection can be tested without faulting a GPU).
+ * Arms the next moe_forward of `ctx` (FP8-weight format only): every pipeline
+ * wait of that forward gives up after `wait_limit_us` microseconds instead of
+ * 2 s, and CTA 0's copy producer in GEMM `which` (1 = L1, 2 = L2) never fills
+ * its first pipeline stage, so the MMA's wait for it runs out.  That forward
+ * returns MOE_OK; its output is undefined; moe_device_status() then returns
+ * MOE_ERR_DEVICE_TIMEOUT, and later forwards run normally.  The hook disarms
+ * itself after one forward.  Returns MOE_ERR_INVALID_ARG for another `which`
+ * or a limit below 1 us, MOE_ERR_UNSUPPORTED for FP4 weights. */
+MOE_API int moe_test_arm_timeout(moe_ctx *ctx, int which, int wait_limit_us);
+
 /* Synchronise the device, read and clear the device error word:
  * MOE_OK, MOE_ERR_BAD_EXPERT, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_CUDA. */
 MOE_API int moe_device_status(moe_ctx *ctx);

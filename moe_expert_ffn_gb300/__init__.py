@@ -33,8 +33,8 @@ MOE_W_FP4_E2M1_UE8M0_32 = 1
 ABI_SYMBOLS = (
     "moe_workspace_bytes", "moe_weight_bytes", "moe_create", "moe_transform_weights",
     "moe_forward", "moe_forward_host", "moe_get_dispatch", "moe_get_intermediates",
-    "moe_dispatch_noalloc", "moe_profile_begin", "moe_profile_end", "moe_device_status",
-    "moe_strerror", "moe_destroy",
+    "moe_dispatch_noalloc", "moe_profile_begin", "moe_profile_end", "moe_test_arm_timeout",
+    "moe_device_status", "moe_strerror", "moe_destroy",
 )
 
 
@@ -85,6 +85,8 @@ def lib():
             L.moe_profile_begin.argtypes = [vp, i32]
             L.moe_profile_end.restype = i32
             L.moe_profile_end.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+            L.moe_test_arm_timeout.restype = i32
+            L.moe_test_arm_timeout.argtypes = [vp, i32, i32]
             L.moe_device_status.restype = i32
             L.moe_device_status.argtypes = [vp]
             L.moe_strerror.restype = ctypes.c_char_p
@@ -245,6 +247,11 @@ class MoELayer:
 
     def device_status(self) -> int:
         return int(lib().moe_device_status(self._ctx))
+
+    def arm_timeout_test(self, which: int, wait_limit_us: int):
+        """Make the next forward's GEMM `which` (1 = L1, 2 = L2) time out on
+        purpose after `wait_limit_us` (a test of the failure path)."""
+        _check(lib().moe_test_arm_timeout(self._ctx, int(which), int(wait_limit_us)), "moe_test_arm_timeout")
 
     def close(self):
         if getattr(self, "_ctx", None):

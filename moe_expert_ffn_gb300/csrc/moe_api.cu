@@ -162,6 +162,8 @@ struct moe_ctx {
     AMaps tm_l2a, tm_pool;
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     int l1_pair_mode;       // 0 auto, 1 CTA pairs, 2 single CTAs
+    int test_hook[2];       // armed timeout test for the next forward: {limit us, stall target}
+    bool test_armed;
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
     int prof_max, prof_n;
 
@@ -271,6 +273,9 @@ int moe_transform_weights(moe_ctx *c, const void *w1, const void *w1_sf, const v
     return MOE_OK;
 }
 
+static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_t *topk_idx,
+                            const float *topk_weights, void *y, int32_t *stats, cudaStream_t s);
+
 int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_t *topk_idx,
                 const float *topk_weights, void *y, int32_t *stats, void *stream) {
     if (!c) return MOE_ERR_INVALID_ARG;
@@ -283,10 +288,25 @@ int moe_forward(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_
         !aligned(topk_weights, 4) || (stats && !aligned(stats, 4)))
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout &L = c->L;
+    // timeout-path test hook: words 1-2 of the error block for this forward only
+    const bool test = c->test_armed;
+    c->test_armed = false;
+    if (test && cudaMemcpyAsync(c->ws + L.err + sizeof(int), c->test_hook, 2 * sizeof(int),
+                                cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int rc = forward_launches(c, T, x, x_sf, topk_idx, topk_weights, y, stats, s);
+    if (test && cudaMemsetAsync(c->ws + L.err + sizeof(int), 0, 2 * sizeof(int), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return rc;
+}
+
+static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, const int32_t *topk_idx,
+                            const float *topk_weights, void *y, int32_t *stats, cudaStream_t s) {
+    const moe_config &g = c->cfg;
     const int E = g.num_experts, H = g.hidden, I = g.inter, k = g.topk;
     const int Pm = g.max_tokens * k;
     const Layout &L = c->L;
-
     DispatchOut o;
     o.count = c->w<int32_t>(L.count);
     o.offset = c->w<int32_t>(L.offset);
@@ -504,6 +524,15 @@ int moe_profile_end(moe_ctx *c, float *stage_ms, int *n_forwards) {
     if (n_forwards) *n_forwards = c->prof_n;
     profile_release(c);
     return rc;
+}
+
+int moe_test_arm_timeout(moe_ctx *c, int which, int wait_limit_us) {
+    if (!c || (which != kStallL1 && which != kStallL2) || wait_limit_us < 1) return MOE_ERR_INVALID_ARG;
+    if (c->cfg.wfmt != MOE_W_FP8_BLK128) return MOE_ERR_UNSUPPORTED;
+    c->test_hook[0] = wait_limit_us;
+    c->test_hook[1] = which;
+    c->test_armed = true;
+    return MOE_OK;
 }
 
 int moe_device_status(moe_ctx *c) {

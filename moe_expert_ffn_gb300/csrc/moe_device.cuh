@@ -16,6 +16,13 @@ constexpr int kErrTimeout = 2;
 // A pipeline wait gives up after this long (a healthy wait lasts microseconds).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
+// The device error block (4 ints in the workspace): [0] error bits, [1] wait
+// limit in microseconds for a test of the timeout path (0 = kWaitTimeoutNs),
+// [2] test stall target (kStallL1 / kStallL2: CTA 0's producer in that GEMM
+// withholds the copies of its first stage), [3] unused.
+constexpr int kStallL1 = 1;
+constexpr int kStallL2 = 2;
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -87,10 +94,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           int *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const int lim_us = reinterpret_cast<volatile int *>(err)[1];
+    const uint64_t limit = lim_us > 0 ? 1000ull * (uint64_t)lim_us : kWaitTimeoutNs;
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(err, kErrTimeout);
             return false;

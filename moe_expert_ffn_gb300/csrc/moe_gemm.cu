@@ -121,9 +121,9 @@ __device__ __forceinline__ void release_tbuf(Ctrl *ctrl, int b, uint32_t lane) {
 }
 
 // After a failed wait: let the producer's issued copies land before exit.
-__device__ __forceinline__ void drain_producer(Ctrl *ctrl, int it, int stages) {
+__device__ __forceinline__ void drain_producer(Ctrl *ctrl, int it, int stages, const int *err) {
     for (int i = max(0, it - stages); i < it; ++i)
-        drain_wait(smem_u32(&ctrl->full[i % stages]), (i / stages) & 1);
+        drain_wait(smem_u32(&ctrl->full[i % stages]), (i / stages) & 1, err);
 }
 
 // Promote this warp's 128 columns (TMEM columns tcol..tcol+127 of the
@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         const uint64_t pol_once = policy_evict_first();
         const uint64_t pol_shared = policy_evict_normal();
         const uint64_t pol_x = policy_evict_last();
+        const bool stall = test_stall(p.err, kStallL1);
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
                     ok = false;
                     break;
                 }
+                if (stall && it == 0) continue;   // timeout-path test: never fill stage 0
                 const uint32_t full = smem_u32(&ctrl->full[s]);
                 if (lane == 0) mbar_arrive_expect_tx(full, tx);
                 __syncwarp();
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
                                 pol_w);
             }
         }
-        if (!ok) drain_producer(ctrl, it, kL1Stages);
+        if (!ok) drain_producer(ctrl, it, kL1Stages, p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
             }
         }
         if (!ok && it > 0)
-            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kL1Stages]), ((it - 1) / kL1Stages) & 1);
+            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kL1Stages]), ((it - 1) / kL1Stages) & 1, p.err);
     } else {
         // ---------------- epilogue ----------------
         const int q = warp & 3;                  // TMEM lane quadrant this warp may access
@@ -386,6 +388,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
             const uint64_t pol_once = policy_evict_first();
             const uint64_t pol_shared = policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
+            const bool stall = test_stall(p.err, kStallL2);
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
                         ok = false;
                         break;
                     }
+                    if (stall && it == 0) continue;   // timeout-path test: never fill stage 0
                     const uint32_t full = smem_u32(&ctrl->full[s]);
                     const int abox = a_box_index(t.rows);
                     mbar_arrive_expect_tx(full, (32u << abox) * kBK + kL2BBytes);
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
                                 pol_w);
                 }
             }
-            if (!ok) drain_producer(ctrl, it, kL2Stages);
+            if (!ok) drain_producer(ctrl, it, kL2Stages, p.err);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
             }
         }
         if (!ok && kt > 0)
-            drain_wait(smem_u32(&ctrl->tfull[(kt - 1) % kL2TBufs]), ((kt - 1) / kL2TBufs) & 1);
+            drain_wait(smem_u32(&ctrl->tfull[(kt - 1) % kL2TBufs]), ((kt - 1) / kL2TBufs) & 1, p.err);
     } else {
         const int q = warp & 3;
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns

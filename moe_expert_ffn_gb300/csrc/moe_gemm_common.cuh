@@ -47,11 +47,20 @@ __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) &
 // Index of the smallest A box (32, 64 or 128 rows) covering `rows` rows.
 __device__ __forceinline__ int a_box_index(int rows) { return rows <= 32 ? 0 : (rows <= 64 ? 1 : 2); }
 
-// Bounded wait used only on the abort path (does not look at the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait used only on the abort path (does not look at the abort flag;
+// same limit as mbar_wait).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const int *err) {
+    const int lim_us = reinterpret_cast<const volatile int *>(err)[1];
+    const uint64_t limit = lim_us > 0 ? 1000ull * (uint64_t)lim_us : kWaitTimeoutNs;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+        if (globaltimer_ns() - t0 > limit) return;
+}
+
+// Test of the timeout path: whether CTA 0's producer in GEMM `which` withholds
+// the copies of its first stage (so the MMA's wait for them runs out).
+__device__ __forceinline__ bool test_stall(const int *err, int which) {
+    return blockIdx.x == 0 && reinterpret_cast<const volatile int *>(err)[2] == which;
 }
 
 

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok)
             for (int i = max(0, it - kStages); i < it; ++i)
-                drain_wait(smem_u32(&ctrl->full[i % kStages]), (i / kStages) & 1);
+                drain_wait(smem_u32(&ctrl->full[i % kStages]), (i / kStages) & 1, p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         int it = 0, tc = 0;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok && it > 0)
-            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1);
+            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1, p.err);
     } else if (warp < kEpiWarp0) {
         // ---------------- scale writers ----------------
         const int q = warp & 3;

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the copies of the last stages must land before the pair tears down
         for (int i = max(0, it - kStages); i < it; ++i)
-            drain_wait(smem_u32(&ctrl->empty[i % kStages]), (i / kStages) & 1);
+            drain_wait(smem_u32(&ctrl->empty[i % kStages]), (i / kStages) & 1, p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer (even CTA) ----------------
         if (leader) {
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
             }
-            if (it > 0) drain_wait(smem_u32(&ctrl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1);
+            if (it > 0) drain_wait(smem_u32(&ctrl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1, p.err);
         }
     } else {
         // ---------------- epilogue (both CTAs, own 128 rows) ----------------

@@ -49,5 +49,6 @@ def test_sizes_and_host_checks(lib):
     assert L.moe_create(ctypes.byref(ctx), ctypes.byref(cfg), None, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_forward(None, 1, None, None, None, None, None, None, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_device_status(None) == lib.MOE_ERR_INVALID_ARG
+    assert L.moe_test_arm_timeout(None, 1, 1000) == lib.MOE_ERR_INVALID_ARG
     assert lib.strerror(lib.MOE_ERR_BAD_EXPERT).startswith("topk_idx")
     L.moe_destroy(None)

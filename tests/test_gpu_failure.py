@@ -1,0 +1,62 @@
+"""Failure detection on the GPU without a GPU fault.
+
+A test hook (moe_test_arm_timeout) makes one forward's GEMM wait for a
+pipeline stage that its producer never fills, with every wait limited to a
+few milliseconds: the bounded wait must give up, the kernel must drain its
+copies, free its tensor memory and return, the host must read
+MOE_ERR_DEVICE_TIMEOUT, and the next forward on the same context must be
+correct again.  Nothing faults, traps or hangs.
+"""
+import time
+
+import pytest
+import torch
+
+import moe_synth
+from gpu_util import new_layer, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_ffn_gb300 import build
+    build.build()
+    import moe_expert_ffn_gb300 as mod
+    return mod
+
+
+@pytest.mark.parametrize("which", [1, 2], ids=["l1", "l2"])
+def test_timeout_is_reported_and_context_recovers(m, which):
+    wl = moe_synth.custom(T=96, H=512, I=256, E=4, k=2, seed=71)
+    inp = to_dev(moe_synth.make_inputs(wl), DEV)
+    layer = new_layer(m, wl, DEV)
+    layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    args = (inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
+    y0 = layer.forward(*args).clone()
+    assert layer.device_status() == m.MOE_OK
+
+    layer.arm_timeout_test(which, 20000)          # 20 ms limit per wait
+    t0 = time.monotonic()
+    layer.forward(*args)
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert layer.device_status() == m.MOE_ERR_DEVICE_TIMEOUT
+    assert elapsed < 5.0, elapsed                  # gave up, did not wait the default 2 s per wait
+
+    # the status read cleared the error word; the context is usable and exact again
+    y1 = layer.forward(*args)
+    assert layer.device_status() == m.MOE_OK
+    assert torch.equal(y1, y0)
+
+
+def test_arm_rejects_bad_arguments(m):
+    wl = moe_synth.WORKLOADS["tiny"]
+    layer = new_layer(m, wl, DEV)
+    for which, lim in ((0, 1000), (3, 1000), (1, 0)):
+        with pytest.raises(m.MoEError):
+            layer.arm_timeout_test(which, lim)
