@@ -205,8 +205,8 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     const bool fp4 = g.wfmt == MOE_W_FP4_E2M1_UE8M0_32;
     const CUtensorMapDataType packed = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
     const Layout &L = c->L;
-    bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128, packed) &&
-                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 128, packed)
+    bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256, packed) &&
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256, packed)
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
                          make_map(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256));

@@ -18,20 +18,23 @@
 // Weight tiles are loaded by TMA straight from the packed codes: the tensor
 // map type 16U4_ALIGN16B expands every 16 codes (8 bytes) into a 16-byte slot,
 // the layout the f8f6f4 MMA reads for E2M1, so HBM moves half a byte per
-// weight.  Tiles are 128 rows x 128 columns, K stages of 128.  Warp roles, 10
-// warps:
-//   warp 0     TMA producer (6 stages: A 16 KB, B 16 KB);
+// weight.  Such a copy costs an SM about the same time whether its box has
+// 128 or 256 rows, so tiles are 128 rows x 256 columns (one 256-row weight
+// box per stage), K stages of 128.  Warp roles, 10 warps:
+//   warp 0     TMA producer (4 stages: A 16 KB, B 32 KB);
 //   warp 1     TMEM allocation, then MMA issuer;
 //   warps 2-5  scale writers: for every stage they load the UE8M0 words (four
-//              K steps per 32-bit word) of the tile's 128 A rows and 128 B rows
+//              K steps per 32-bit word) of the tile's 128 A rows and 256 B rows
 //              and tcgen05.st them into a TMEM slot of the scale ring.  The MMA
 //              reads the scale of row r from TMEM lane 32*(m/32) + r%32 (m =
 //              the output row being computed), column base + r/32, so each lane
 //              quadrant holds a full copy: lane 32q + j, column base + c = row
 //              32c + j;
-//   warps 6-9  epilogue, one per TMEM lane quadrant, 128 columns per thread:
-//              two accumulators in TMEM let the next tile's MMAs run while the
-//              epilogue drains the previous one.
+//   warps 6-9  epilogue, one per TMEM lane quadrant: each thread reads its
+//              row's 256 accumulator columns in two halves of 128 (64 gate/up
+//              pairs, or 128 outputs), frees the accumulator after the second
+//              read, and converts and stores each half.  One 256-column
+//              accumulator plus the scale ring fit in TMEM.
 #include "moe_device.cuh"
 #include "moe_gemm_common.cuh"
 #include "moe_internal.h"
@@ -40,16 +43,18 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kBN = 128;
-constexpr int kStages = 6;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
 constexpr uint32_t kABytes = kBM * kBK;
 constexpr uint32_t kBBytes = kBN * kBK;                 // E2M1 expanded to one byte per code
 constexpr uint32_t kBTxBytes = kBN * kBK / 2;           // a 16U4 load counts the packed bytes
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kAccs = 2;                                // 128-column accumulators
+constexpr int kAccs = 1;                                // 256-column accumulators
 constexpr uint32_t kSfCol0 = kAccs * kBN;               // scale ring after the accumulators
-constexpr uint32_t kSfSlotCols = 8;                     // 4 columns A scales + 4 columns B scales
+constexpr uint32_t kSfACols = kBM / 32;                 // A scales: one column per 32 rows
+constexpr uint32_t kSfSlotCols = 16;                    // then B scales (8 columns); 16-aligned slots
+static_assert(kSfACols + kBN / 32 <= kSfSlotCols, "scale slot");
 constexpr int kNumSfWarps = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kEpiWarp0 = 6;                           // warps 2..5 write scales
@@ -95,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
-    const int NB = kL1 ? 2 * p.I / kBN : p.H / kBN;
+    // N blocks: L1 covers the 2I interleaved rows exactly; L2's last block is
+    // half empty when H % 256 == 128
+    const int NB = kL1 ? 2 * p.I / kBN : (p.H + kBN - 1) / kBN;
     const int KB = kL1 ? p.H / kBK : p.I / kBK;
     const int brow0 = kL1 ? 2 * p.I : p.H;          // B rows per expert
     const int sf_row_bytes = (kL1 ? p.H : p.I) / 32; // scale bytes per row of A and B
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 32; ++kk)
                         umma_mx(tmem + b * kBN, ad + 2 * kk, bd + 2 * kk, idesc_mx_e4m3_e2m1(kBM, kBN, kk),
-                                sfa, sfa + 4, (kb | kk) != 0);
+                                sfa, sfa + kSfACols, (kb | kk) != 0);
                     umma_commit(smem_u32(&ctrl->empty[s]));
                     umma_commit(smem_u32(&ctrl->sf_empty[s]));
                     if (kb == KB - 1) umma_commit(smem_u32(&ctrl->acc_full[b]));
@@ -218,9 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
-            // row c*32 + lane of the tile, for c = 0..3 (A: pool rows, B: weight rows)
+            // row c*32 + lane of the tile: A pool rows c = 0..3, B weight rows
+            // c = 0..7 (rows past the expert's last weight row, in a half-empty
+            // L2 block, reuse that row: their outputs are masked)
             const uint8_t *arow[4];
-            const uint8_t *brow[4];
+            const uint8_t *brow[8];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int r = 32 * c + (int)lane;
@@ -229,25 +238,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     arow[c] = p.a_sf + (size_t)(__ldg(p.gather + prow) / p.k) * sf_row_bytes;
                 else
                     arow[c] = p.a_sf + (size_t)prow * sf_row_bytes;
-                brow[c] = p.b_sf + (size_t)(t.e * brow0 + t.nb * kBN + r) * sf_row_bytes;
             }
-            uint32_t wa[4], wb[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                wa[c] = ld_u32(arow[c]);
-                wb[c] = ld_u32(brow[c]);
+            for (int c = 0; c < 8; ++c) {
+                const int r = min(t.nb * kBN + 32 * c + (int)lane, brow0 - 1);
+                brow[c] = p.b_sf + (size_t)(t.e * brow0 + r) * sf_row_bytes;
             }
+            uint32_t wa[4], wb[8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) wa[c] = ld_u32(arow[c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) wb[c] = ld_u32(brow[c]);
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
                 // words of the next K block, loaded while this one is stored
-                uint32_t na[4], nbw[4];
+                uint32_t na[4], nbw[8];
                 const int kn = min(kb + 1, KB - 1) * 4;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    na[c] = ld_u32(arow[c] + kn);
-                    nbw[c] = ld_u32(brow[c] + kn);
-                }
+                for (int c = 0; c < 4; ++c) na[c] = ld_u32(arow[c] + kn);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) nbw[c] = ld_u32(brow[c] + kn);
                 if (!mbar_wait(smem_u32(&ctrl->sf_empty[s]), ph ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -255,16 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t col = t_lane + s * kSfSlotCols;
                 tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
-                tmem_st4(col + 4, wb[0], wb[1], wb[2], wb[3]);
+                tmem_st4(col + kSfACols, wb[0], wb[1], wb[2], wb[3]);
+                tmem_st4(col + kSfACols + 4, wb[4], wb[5], wb[6], wb[7]);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ctrl->sf_full[s]));
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    wa[c] = na[c];
-                    wb[c] = nbw[c];
-                }
+                for (int c = 0; c < 4; ++c) wa[c] = na[c];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) wb[c] = nbw[c];
             }
         }
     } else {
@@ -284,75 +295,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool valid = lrow < t.rows;
             const bool warp_on = q * 32 < t.rows;
-            float acc[128];
-            if (warp_on) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tmem_ld32(t_lane + b * kBN + 32 * c, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[32 * c + i] = v[i];
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[b]));
-            if (!valid) continue;
             const int row = t.row0 + lrow;
-            if (kL1) {
-                // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
-                const float wgt = __ldg(p.topk_w + __ldg(p.gather + row));
-                const float clampv = p.clamp;
+            // the row's 256 columns in two halves of 128; the accumulator is
+            // freed once the second half is in registers
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int cb = t.nb * 2 + h;   // 128-column block of the output
+                float acc[128];
+                if (warp_on) {
 #pragma unroll
-                for (int o = 0; o < 64; ++o) {
-                    const int gi = 16 * (o >> 3) + (o & 7);
-                    const float g = fminf(fmaxf(acc[gi], -clampv), clampv);
-                    const float u = fminf(fmaxf(acc[gi + 8], -clampv), clampv);
-                    float silu;
-                    if (kFast)
-                        silu = __fdividef(g, 1.0f + __expf(-g));
-                    else
-                        silu = __fdividef(g, 1.0f + expf(-g));
-                    acc[gi] = silu * u * wgt;
-                }
-                // two 32-column groups, UE8M0 scale 2^ceil(log2(amax/448)) each
-                uint32_t pk[16];
-                uint32_t codes = 0;
+                    for (int c = 0; c < 4; ++c) {
+                        float v[32];
+                        tmem_ld32(t_lane + b * kBN + h * 128 + 32 * c, v);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int grp = 0; grp < 2; ++grp) {
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int o = 32 * grp; o < 32 * grp + 32; ++o)
-                        amax = fmaxf(amax, fabsf(acc[16 * (o >> 3) + (o & 7)]));
-                    const int e = ue8m0_exponent(amax);
-                    // a / 2^e as a * 2^-e: both exact powers of two, the same rounding
-                    const float rsf = ldexpf(1.0f, -e);
-                    codes |= static_cast<uint32_t>(e + 127) << (8 * grp);
-#pragma unroll
-                    for (int w4 = 8 * grp; w4 < 8 * grp + 8; ++w4) {
-                        float qv[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int o = w4 * 4 + j;
-                            const float a = acc[16 * (o >> 3) + (o & 7)];
-                            qv[j] = (amax == 0.0f) ? 0.0f : a * rsf;
-                        }
-                        pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
+                        for (int i = 0; i < 32; ++i) acc[32 * c + i] = v[i];
                     }
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + t.nb * 64);
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[b]));
+                }
+                if (!valid) continue;
+                if (kL1) {
+                    // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
+                    const float wgt = __ldg(p.topk_w + __ldg(p.gather + row));
+                    const float clampv = p.clamp;
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                *reinterpret_cast<uint16_t *>(p.l2_sf + (size_t)row * (p.I / 32) + 2 * t.nb) =
-                    static_cast<uint16_t>(codes);
-            } else {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + t.nb * kBN);
+                    for (int o = 0; o < 64; ++o) {
+                        const int gi = 16 * (o >> 3) + (o & 7);
+                        const float g = fminf(fmaxf(acc[gi], -clampv), clampv);
+                        const float u = fminf(fmaxf(acc[gi + 8], -clampv), clampv);
+                        float silu;
+                        if (kFast)
+                            silu = __fdividef(g, 1.0f + __expf(-g));
+                        else
+                            silu = __fdividef(g, 1.0f + expf(-g));
+                        acc[gi] = silu * u * wgt;
+                    }
+                    // two 32-column groups, UE8M0 scale 2^ceil(log2(amax/448)) each
+                    uint32_t pk[16];
+                    uint32_t codes = 0;
 #pragma unroll
-                for (int v = 0; v < 16; ++v)
-                    dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]), bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                                        bf16x2(acc[8 * v + 4], acc[8 * v + 5]), bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+                    for (int grp = 0; grp < 2; ++grp) {
+                        float amax = 0.0f;
+#pragma unroll
+                        for (int o = 32 * grp; o < 32 * grp + 32; ++o)
+                            amax = fmaxf(amax, fabsf(acc[16 * (o >> 3) + (o & 7)]));
+                        const int e = ue8m0_exponent(amax);
+                        // a / 2^e as a * 2^-e: both exact powers of two, the same rounding
+                        const float rsf = ldexpf(1.0f, -e);
+                        codes |= static_cast<uint32_t>(e + 127) << (8 * grp);
+#pragma unroll
+                        for (int w4 = 8 * grp; w4 < 8 * grp + 8; ++w4) {
+                            float qv[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int o = w4 * 4 + j;
+                                const float a = acc[16 * (o >> 3) + (o & 7)];
+                                qv[j] = (amax == 0.0f) ? 0.0f : a * rsf;
+                            }
+                            pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
+                        }
+                    }
+                    // outputs [64 cb, 64 cb + 64) of the intermediate dimension
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + cb * 64);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    *reinterpret_cast<uint16_t *>(p.l2_sf + (size_t)row * (p.I / 32) + 2 * cb) =
+                        static_cast<uint16_t>(codes);
+                } else if (cb * 128 < p.H) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + cb * 128);
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        dst[v] = make_uint4(bf16x2(acc[8 * v + 0], acc[8 * v + 1]),
+                                            bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                                            bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
+                                            bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+                }
             }
         }
     }
