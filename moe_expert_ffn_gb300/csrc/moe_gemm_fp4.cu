@@ -30,11 +30,13 @@
 //              the output row being computed), column base + r/32, so each lane
 //              quadrant holds a full copy: lane 32q + j, column base + c = row
 //              32c + j;
-//   warps 6-9  epilogue, one per TMEM lane quadrant: each thread reads its
-//              row's 256 accumulator columns in two halves of 128 (64 gate/up
-//              pairs, or 128 outputs), frees the accumulator after the second
-//              read, and converts and stores each half.  One 256-column
-//              accumulator plus the scale ring fit in TMEM.
+//   warps 6-9  epilogue, one per TMEM lane quadrant: each thread moves the
+//              first 128 of its row's 256 accumulator columns to a TMEM stash,
+//              reads the second 128 into registers and frees the accumulator
+//              (so the next tile's MMAs start after two copies, not after the
+//              conversion), then converts and stores each half (64 gate/up
+//              pairs, or 128 outputs).  One 256-column accumulator, the scale
+//              ring and the stash fit in TMEM.
 #include "moe_device.cuh"
 #include "moe_gemm_common.cuh"
 #include "moe_internal.h"
@@ -55,10 +57,11 @@ constexpr uint32_t kSfCol0 = kAccs * kBN;               // scale ring after the 
 constexpr uint32_t kSfACols = kBM / 32;                 // A scales: one column per 32 rows
 constexpr uint32_t kSfSlotCols = 16;                    // then B scales (8 columns); 16-aligned slots
 static_assert(kSfACols + kBN / 32 <= kSfSlotCols, "scale slot");
+constexpr uint32_t kStashCol0 = kSfCol0 + kStages * kSfSlotCols;   // 128 columns: the epilogue's first half
 constexpr int kNumSfWarps = 4;
 constexpr int kNumEpiWarps = 4;
 constexpr int kEpiWarp0 = 6;                           // warps 2..5 write scales
-static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "TMEM budget");
+static_assert(kStashCol0 + 128 <= kTmemCols, "TMEM budget");
 
 struct alignas(8) Ctrl {
     uint64_t full[kStages];
@@ -296,26 +299,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = lrow < t.rows;
             const bool warp_on = q * 32 < t.rows;
             const int row = t.row0 + lrow;
-            // the row's 256 columns in two halves of 128; the accumulator is
-            // freed once the second half is in registers
+            // first half -> stash, second half -> registers, free the accumulator
+            float acc[128];
+            if (warp_on) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32(t_lane + b * kBN + 32 * c, v);
+                    tmem_ld_wait();
+                    tmem_st32(t_lane + kStashCol0 + 32 * c, v);
+                }
+                tmem_st_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_ld32(t_lane + b * kBN + 128 + 32 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * c + i] = v[i];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[b]));
+            // convert the second half (in registers), then the first (from the stash)
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            for (int pass = 0; pass < 2; ++pass) {
+                const int h = 1 - pass;
                 const int cb = t.nb * 2 + h;   // 128-column block of the output
-                float acc[128];
-                if (warp_on) {
+                if (pass == 1 && warp_on) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float v[32];
-                        tmem_ld32(t_lane + b * kBN + h * 128 + 32 * c, v);
+                        tmem_ld32(t_lane + kStashCol0 + 32 * c, v);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) acc[32 * c + i] = v[i];
                     }
-                }
-                if (h == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[b]));
                 }
                 if (!valid) continue;
                 if (kL1) {
