@@ -139,6 +139,22 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same rows as a 3-D tensor [inner/128 panels][outer rows][128 bytes], so
+// that one box of box_panels panels x box_outer rows fetches several 128-byte
+// K panels of the same rows (each panel a separate 128-byte-swizzled tile).
+bool make_map_panels(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
+                     uint32_t box_outer, uint32_t box_panels) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || inner % 128) return false;
+    cuuint64_t dims[3] = {128, outer, inner / 128};
+    cuuint64_t strides[2] = {stride, 128};
+    cuuint32_t box[3] = {128, box_outer, box_panels};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Bytes of the activation scales of T tokens.
@@ -158,7 +174,8 @@ struct moe_ctx {
     bool weights_ready;
     int last_T;
     CUtensorMap tm_w1, tm_w2;
-    CUtensorMap tm_w1h;     // FP8 W1i with 128-row boxes (CTA-pair L1)
+    CUtensorMap tm_w1h;     // FP8 W1i as K panels, 128 rows x 2 panels per box (CTA-pair L1)
+    CUtensorMap tm_pool3;   // the pool the same way
     AMaps tm_l2a, tm_pool;
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     int l1_pair_mode;       // 0 auto, 1 CTA pairs, 2 single CTAs
@@ -208,7 +225,8 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     bool ok = (fp4 ? make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256, packed) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256, packed)
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
-                         make_map(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 128) &&
+                         make_map_panels(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 2) &&
+                         make_map_panels(&c->tm_pool3, c->ws + L.pool, H, Pm, L.pool_pitch, 128, 2) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256));
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
@@ -390,10 +408,10 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     p1.clamp = g.act_clamp;
     // CTA pairs only on request for now (MOE_L1_PAIR=1): single CTAs are
     // faster end to end on every measured workload
-    const bool pair = c->l1_pair_mode == 1;
+    const bool pair = c->l1_pair_mode == 1 && H % 256 == 0;
     if (pair) {
-        if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_w1h, p1, g.fast_math, gather_a, c->num_sms, s) !=
-            cudaSuccess)
+        if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_pool3, c->tm_w1h, p1, g.fast_math, gather_a,
+                           c->num_sms, s) != cudaSuccess)
             return MOE_ERR_CUDA;
     } else {
         launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);

@@ -121,6 +121,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// 3-D box {x, y, z} into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                            uint32_t bar, uint64_t cache_hint) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(cache_hint)
+        : "memory");
+}
+
 // Prefetch a 2-D box into L2 (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(x),
@@ -326,6 +336,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tm), "r"(x), "r"(y), "r"(bar_cluster), "l"(cache_hint)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                                 uint32_t bar_cluster, uint64_t cache_hint) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "l"(cache_hint)
         : "memory");
 }
 __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap *tm, int x, int r0, int r1,

@@ -8,7 +8,10 @@
 // pool rows and half of the 256 weight rows, and one M=256 MMA issued by the
 // even CTA reads both CTAs' halves.  Every SM then receives 32 KB per 128-K
 // block instead of 48 KB for the same tensor work; the copy bandwidth into an
-// SM, not the tensor core, is what bounds the one-CTA kernel.
+// SM, not the tensor core, is what bounds the one-CTA kernel.  A stage holds
+// two 128-K blocks (64 KB per CTA, 3 stages): the copy rate into an SM grows
+// with the bytes a stage moves (about 70 B/clk at 64 KB against 40-48 at
+// 32 KB), and the weight half arrives as one 3-D box of two K panels.
 //
 // Each CTA's TMEM holds the accumulators of its own 128 rows over all 256
 // columns, so the epilogue is the one-CTA epilogue.  Barriers: the even CTA
@@ -30,9 +33,12 @@ constexpr int kBN = 256;             // tile columns (interleaved gate/up rows o
 constexpr int kHalfBN = kBN / 2;     // weight rows staged by each CTA
 constexpr int kPairRows = 2 * kBM;   // pool rows of a pair tile
 constexpr int kTBufs = 2;
-constexpr int kStages = 6;
-constexpr uint32_t kABytes = kBM * kBK;       // this CTA's 128 pool rows
-constexpr uint32_t kBBytes = kHalfBN * kBK;   // this CTA's 128 weight rows
+constexpr int kStages = 3;
+constexpr int kPanels = 2;                          // 128-K blocks per stage
+constexpr uint32_t kAPanel = kBM * kBK;             // this CTA's 128 pool rows, one block
+constexpr uint32_t kBPanel = kHalfBN * kBK;         // this CTA's 128 weight rows, one block
+constexpr uint32_t kABytes = kPanels * kAPanel;
+constexpr uint32_t kBBytes = kPanels * kBPanel;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint16_t kPairMask = 3;
 
@@ -119,10 +125,13 @@ __device__ __forceinline__ uint32_t a_copy_bytes(int rows) {
     return kGatherA ? (uint32_t)((rows + 3) >> 2) * 4 * kBK : (32u << a_box_index(rows)) * kBK;
 }
 
+// tm_a: 2-D maps (gather4 rows of x, or pool boxes of 32/64/128 rows);
+// tm_a3: the pool as [K panel][row][128 B] with 128-row x 2-panel boxes;
+// tm_w1h: W1i the same way (128 weight rows x 2 panels).  H % 256 == 0.
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
-    l1_pair_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1h,
-                   const L1Params p) {
+    l1_pair_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_a3,
+                   const __grid_constant__ CUtensorMap tm_w1h, const L1Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
@@ -134,12 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     const int NB = p.I / 128;   // 256-row blocks of the interleaved 2I rows
-    const int KB = p.H / kBK;
+    const int KB = p.H / kBK;   // 128-K blocks (even)
+    const int KS = KB / kPanels; // stages per tile
     const int total = __ldg(p.mb2_prefix + p.E) * NB;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a.box[0]);
         tma_prefetch_desc(&tm_a.box[2]);
+        tma_prefetch_desc(&tm_a3);
         tma_prefetch_desc(&tm_w1h);
     }
     if (threadIdx.x == 0) {
@@ -191,8 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int wrow = t.e * 2 * p.I + t.nb * kBN + (int)rank * kHalfBN;
             const int n_g4 = (mine + 3) >> 2;
             const int abox = a_box_index(max(mine, 1));
-            const uint32_t tx = a_copy_bytes<kGatherA>(mine) + a_copy_bytes<kGatherA>(peer) + 2 * kBBytes;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            const uint32_t tx =
+                kPanels * (a_copy_bytes<kGatherA>(mine) + a_copy_bytes<kGatherA>(peer)) + 2 * kBBytes;
+            for (int ks = 0; ks < KS; ++ks, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
                 if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort_flag, p.err)) {
@@ -205,14 +217,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = base + s * kStageBytes;
                 if (mine > 0) {
                     if (kGatherA) {
-                        if ((int)lane < n_g4)
-                            tma_gather4_pair(dst + lane * 512, &tm_a.box[0], kb * kBK, tok[0], tok[1], tok[2],
-                                             tok[3], full, pol_x);
+                        if ((int)lane < n_g4) {
+#pragma unroll
+                            for (int j = 0; j < kPanels; ++j)
+                                tma_gather4_pair(dst + j * kAPanel + lane * 512, &tm_a.box[0],
+                                                 (ks * kPanels + j) * kBK, tok[0], tok[1], tok[2], tok[3], full,
+                                                 pol_x);
+                        }
                     } else if (lane == 0) {
-                        tma_load_2d_pair(dst, &tm_a.box[abox], kb * kBK, my_row0, full, pol_x);
+                        if (abox == 2) {   // full rows: both K panels in one 3-D box
+                            tma_load_3d_pair(dst, &tm_a3, 0, my_row0, ks * kPanels, full, pol_x);
+                        } else {           // panel j of a 32/64-row box at the panel's 16 KB slot
+#pragma unroll
+                            for (int j = 0; j < kPanels; ++j)
+                                tma_load_2d_pair(dst + j * kAPanel, &tm_a.box[abox], (ks * kPanels + j) * kBK,
+                                                 my_row0, full, pol_x);
+                        }
                     }
                 }
-                if (lane == 0) tma_load_2d_pair(dst + kABytes, &tm_w1h, kb * kBK, wrow, full, pol_w);
+                if (lane == 0) tma_load_3d_pair(dst + kABytes, &tm_w1h, 0, wrow, ks * kPanels, full, pol_w);
             }
         }
         // the copies of the last stages must land before the pair tears down
@@ -222,29 +245,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer (even CTA) ----------------
         if (leader) {
             constexpr uint32_t idesc = idesc_e4m3_f32(kPairRows, kBN);
-            int it = 0;
+            int it = 0, kt = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < total; tile += npairs) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int ks = 0; ok && ks < KS; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    const int b = it % kTBufs;
-                    const uint32_t tph = (it / kTBufs) & 1;
-                    if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
-                        !mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
+                    if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t ad = sw128_kmajor_desc(base + s * kStageBytes);
-                        const uint64_t bd = sw128_kmajor_desc(base + s * kStageBytes + kABytes);
+                    // each 128-K block of the stage into its own accumulator
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 32; ++kk)
-                            umma_pair_e4m3(tmem + b * kBN, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0);
-                        umma_pair_commit(smem_u32(&ctrl->empty[s]), kPairMask);
-                        umma_pair_commit(smem_u32(&ctrl->tfull[b]), kPairMask);
+                    for (int j = 0; j < kPanels; ++j, ++kt) {
+                        const int b = kt % kTBufs;
+                        const uint32_t tph = (kt / kTBufs) & 1;
+                        if (!mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint64_t ad = sw128_kmajor_desc(base + s * kStageBytes + j * kAPanel);
+                            const uint64_t bd = sw128_kmajor_desc(base + s * kStageBytes + kABytes + j * kBPanel);
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 32; ++kk)
+                                umma_pair_e4m3(tmem + b * kBN, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0);
+                            umma_pair_commit(smem_u32(&ctrl->tfull[b]), kPairMask);
+                        }
+                        __syncwarp();
                     }
+                    if (ok && lane == 0) umma_pair_commit(smem_u32(&ctrl->empty[s]), kPairMask);
                     __syncwarp();
                 }
             }
@@ -350,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t l1_pair_smem_bytes() { return kSmemBytes; }
 
 template <bool kFast, bool kGatherA>
-static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_w1h, const L1Params &p, int num_sms,
-                                 cudaStream_t s) {
+static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
+                                 const L1Params &p, int num_sms, cudaStream_t s) {
     static int grid = 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -376,16 +407,16 @@ static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_w1h, c
         grid = 2 * min(clusters, num_sms / 2);
     }
     cfg.gridDim = dim3(grid);
-    return cudaLaunchKernelEx(&cfg, l1_pair_kernel<kFast, kGatherA>, tm_a, tm_w1h, p);
+    return cudaLaunchKernelEx(&cfg, l1_pair_kernel<kFast, kGatherA>, tm_a, tm_a3, tm_w1h, p);
 }
 
-cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_w1h, const L1Params &p, int fast_math,
-                           bool gather_a, int num_sms, cudaStream_t s) {
+cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
+                           const L1Params &p, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
     if (fast_math)
-        return gather_a ? launch_pair_t<true, true>(tm_a, tm_w1h, p, num_sms, s)
-                        : launch_pair_t<true, false>(tm_a, tm_w1h, p, num_sms, s);
-    return gather_a ? launch_pair_t<false, true>(tm_a, tm_w1h, p, num_sms, s)
-                    : launch_pair_t<false, false>(tm_a, tm_w1h, p, num_sms, s);
+        return gather_a ? launch_pair_t<true, true>(tm_a, tm_a3, tm_w1h, p, num_sms, s)
+                        : launch_pair_t<true, false>(tm_a, tm_a3, tm_w1h, p, num_sms, s);
+    return gather_a ? launch_pair_t<false, true>(tm_a, tm_a3, tm_w1h, p, num_sms, s)
+                    : launch_pair_t<false, false>(tm_a, tm_a3, tm_w1h, p, num_sms, s);
 }
 
 }  // namespace moe

@@ -56,9 +56,11 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, i
                bool gather_a, int num_sms, cudaStream_t s);
 
 // L1 on CTA pairs (moe_gemm_pair.cu): 256 x 256 tiles, one M=256 MMA over
-// both CTAs; tm_w1h maps W1i with 128-row boxes (each CTA stages half a tile).
-cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_w1h, const L1Params &p, int fast_math,
-                           bool gather_a, int num_sms, cudaStream_t s);
+// both CTAs, stages of two 128-K blocks.  tm_a: the 2-D A maps (gather4 from
+// x, or pool boxes); tm_a3 / tm_w1h: the pool / W1i as 3-D [K panel][row][128
+// bytes] with 128-row x 2-panel boxes.  Requires H % 256 == 0.
+cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
+                           const L1Params &p, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
 size_t l1_pair_smem_bytes();
 
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the

@@ -103,7 +103,7 @@ def _crafted_counts(T, k, E, counts, seed):
 # L1 on CTA pairs (256-row blocks): experts whose counts leave the second CTA
 # empty (<= 128), ragged in either half, exactly one or two blocks, several
 # blocks (N-major), plus the generic small cases
-PAIR_CASES = SMALL[1:3] + [moe_synth.custom(T=600, H=384, I=256, E=8, k=2, seed=37, name="pair_counts")]
+PAIR_CASES = SMALL[1:3] + [moe_synth.custom(T=600, H=512, I=256, E=8, k=2, seed=37, name="pair_counts")]
 PAIR_COUNTS = {"pair_counts": [1, 127, 128, 129, 255, 256, 257, 47]}
 
 
