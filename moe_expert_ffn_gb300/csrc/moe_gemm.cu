@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kL1Threads, 1)
             const bool warp_on = q * 32 < t.rows;
             const int row = t.row0 + lrow;
             const int pair = valid ? __ldg(p.gather + row) : 0;
+            // the pair's top-k weight, needed only by the tail: load it now
+            const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
             const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
             const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
             const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
@@ -312,7 +314,6 @@ __global__ void __launch_bounds__(kL1Threads, 1)
             if (!ok || !valid) continue;
 
             // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
-            const float wgt = __ldg(p.topk_w + pair);
             const float clampv = p.clamp;
             float amax = 0.0f;
             float act[64];

@@ -295,6 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_on = (int)rank * kBM + q * 32 < t.rows;
             const int row = t.row0 + lrow;
             const int pair_id = valid ? __ldg(p.gather + row) : 0;
+            // the pair's top-k weight, needed only by the tail: load it now
+            const float wgt = valid ? __ldg(p.topk_w + pair_id) : 0.0f;
             const int jb = t.nb * 2 + h;
             const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
             const float *sfa = p.x_sf + (size_t)(pair_id / p.k) * KB;
@@ -326,7 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok || !valid) continue;
 
-            const float wgt = __ldg(p.topk_w + pair_id);
             const float clampv = p.clamp;
             float amax = 0.0f;
             float act[64];
