@@ -117,6 +117,15 @@ def roofline_for(stage, wm, seconds, peaks, traffic=None):
     return out
 
 
+def launches_per_forward(wl):
+    """Library kernels per forward: dispatch, L1, L2, combine, plus the pool
+    copy when token rows are not gathered inside L1 (the library's rule:
+    gather when T*k <= 4E, unless MOE_L1_A overrides it)."""
+    mode = os.environ.get("MOE_L1_A", "")
+    gather = (mode == "gather") if mode in ("gather", "pool") else wl.T * wl.k <= 4 * wl.E
+    return 4 if gather else 5
+
+
 def profiled_traffic(stage, workload):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload (a line `traffic_bytes_per_launch: N`), or None."""
@@ -372,7 +381,7 @@ def run_ours(args, wl, rank, world, local_rank):
                            "unit": layer_roof["unit"]},
         "roofline": roof,
         "stage_ms": per_launch,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_forward(wl) * args.steps,
         "e2e": e2e,
         "clocks": clk,
     }
@@ -380,7 +389,7 @@ def run_ours(args, wl, rank, world, local_rank):
         import oracle
         oracle.build()
         threads = oracle.num_threads()
-        n_tok = max(1, min(wl.T, 2 * threads))
+        n_tok = max(1, min(wl.T, 6 * threads))       # about 10-15 s of host work
         cin = cpu_sample_inputs(wl, n_tok, seed_offset=1)
         dt = time_oracle(cin, wl.wfmt)
         out["cpu_baseline"] = {"value": n_tok / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
