@@ -484,7 +484,6 @@ int moe_get_intermediates(moe_ctx *c, void *l2_acts, void *l2_sf, void *l2_out, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t H = c->cfg.hidden, I = c->cfg.inter;
     const size_t P = (size_t)c->last_T * c->cfg.topk;
-    const size_t Pm = (size_t)c->cfg.max_tokens * c->cfg.topk;
     if (!P) return MOE_OK;
     if (l2_acts && cudaMemcpy2DAsync(l2_acts, I, c->ws + c->L.l2_acts, c->L.acts_pitch, I, P,
                                      cudaMemcpyDeviceToDevice, s))

@@ -520,8 +520,6 @@ __global__ void __launch_bounds__(kL2Threads, 1)
 
 }  // namespace
 
-size_t l1_smem_bytes() { return kL1SmemBytes; }
-size_t l2_smem_bytes() { return kL2SmemBytes; }
 
 template <bool kFast, bool kGatherA>
 static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,

@@ -379,8 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t l1_pair_smem_bytes() { return kSmemBytes; }
-
 template <bool kFast, bool kGatherA>
 static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
                                  const L1Params &p, int num_sms, cudaStream_t s) {

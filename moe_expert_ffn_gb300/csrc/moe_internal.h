@@ -61,7 +61,6 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, i
 // bytes] with 128-row x 2-panel boxes.  Requires H % 256 == 0.
 cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
                            const L1Params &p, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
-size_t l1_pair_smem_bytes();
 
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
 // first offset[E] rows (rows_bound = T*k is the host-side upper bound).
@@ -112,7 +111,5 @@ void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int
 void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, int w1i_pitch,
                          float2 *w1i_sf, int E, int H, int I, cudaStream_t s);
 
-size_t l1_smem_bytes();
-size_t l2_smem_bytes();
 
 }  // namespace moe
