@@ -134,6 +134,23 @@ def test_l1_cta_pairs_match_oracle(m, orc, wl, a_mode, monkeypatch):
     print(f"{wl.name}/pairs/{a_mode}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
 
 
+@pytest.mark.parametrize("clamp", [float("inf"), 1.0], ids=["noclamp", "clamp1"])
+@pytest.mark.parametrize("fast", [0, 1], ids=["expf", "fastexp"])
+@pytest.mark.parametrize("variant", ["single", "pairs", "fp4"])
+def test_epilogue_options_match_oracle(m, orc, variant, fast, clamp, monkeypatch):
+    """fast_math and the activation clamp in each L1 epilogue (one CTA, CTA
+    pairs, FP4 weights): the clamp of 1.0 clips about a third of the gate/up
+    values of this case, so its branch is exercised."""
+    wfmt = 1 if variant == "fp4" else 0
+    monkeypatch.setenv("MOE_L1_PAIR", "1" if variant == "pairs" else "0")
+    wl = moe_synth.custom(T=300, H=512, I=256, E=8, k=2, seed=81, wfmt=wfmt, name="opts")
+    inp = moe_synth.make_inputs(wl)
+    layer, g, y = _run(m, wl, inp, wfmt=wfmt, act_clamp=clamp, fast_math=bool(fast))
+    ref = bf16_bits_to_float(orc.forward(inp, wfmt=wfmt, act_clamp=clamp))
+    rel, mx = assert_y_close(y, ref, f"{variant}/fast{fast}/clamp{clamp}")
+    print(f"{variant} fast={fast} clamp={clamp}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
+
+
 def test_zero_tokens_and_inactive_slots(m, orc):
     wl = moe_synth.custom(T=40, H=256, I=128, E=8, k=3, seed=35)
     inp = moe_synth.make_inputs(wl)
