@@ -122,12 +122,13 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D tensor [outer, inner] with row stride `stride` bytes, boxes of
-// box_inner x box_outer elements, 128-byte swizzle.  Bytes (box_inner 128),
-// or packed 4-bit codes expanded to one byte each in shared memory
-// (16U4_ALIGN16B: inner counts codes, box_inner 128).
+// box_inner x box_outer elements, 128-byte swizzle unless asked otherwise.
+// Bytes (box_inner 128), 16-bit words, or packed 4-bit codes expanded to one
+// byte each in shared memory (16U4_ALIGN16B: inner counts codes, box_inner 128).
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t stride,
               uint32_t box_inner, uint32_t box_outer,
-              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_UINT8) {
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_UINT8,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -135,7 +136,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
     return fn(m, dtype, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -174,6 +175,7 @@ struct moe_ctx {
     bool weights_ready;
     int last_T;
     CUtensorMap tm_w1, tm_w2;
+    CUtensorMap tm_l2out;   // l2_out [Pmax, H] BF16, 32-row x 64-column boxes (FP8 L2 epilogue stores)
     CUtensorMap tm_w1h;     // FP8 W1i as K panels, 128 rows x 2 panels per box (CTA-pair L1)
     CUtensorMap tm_pool3;   // the pool the same way
     AMaps tm_l2a, tm_pool;
@@ -227,7 +229,9 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
                          make_map_panels(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 2) &&
                          make_map_panels(&c->tm_pool3, c->ws + L.pool, H, Pm, L.pool_pitch, 128, 2) &&
-                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256));
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256) &&
+                         make_map(&c->tm_l2out, c->ws + L.l2_out, H, Pm, H * 2, 64, 32,
+                                  CU_TENSOR_MAP_DATA_TYPE_UINT16));
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
              make_map(&c->tm_pool.box[i], c->ws + L.pool, H, Pm, L.pool_pitch, 128, 32u << i);
@@ -430,7 +434,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     p2.I = I;
     p2.E = E;
     p2.Pmax = Pm;
-    launch_l2(c->tm_l2a, c->tm_w2, p2, c->num_sms, s);
+    launch_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, p2, c->num_sms, s);
     if (ev) cudaEventRecord(ev[3], s);
 
     launch_combine(p2.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);

@@ -25,7 +25,10 @@
 //              columns per warp): tcgen05.ld each finished accumulator,
 //              release it, and FMA it into FP32 registers with its scale
 //              product (the pages' "promotion"); after the last block,
-//              SwiGLU/requantise (L1) or BF16 (L2) and store.
+//              SwiGLU/requantise (L1) or BF16 (L2) and store.  The L2 output
+//              goes through a per-warp shared-memory box and a TMA store, so
+//              each row leaves as whole 128-byte pieces instead of 32 rows'
+//              16-byte pieces per instruction.
 // L1: 128 x 256 tiles (128 gate/up pairs = two 64-column output groups), two
 // 256-column accumulators, one per 128-K block.  L2: 128 x 256 tiles, two
 // 256-column accumulators, one per 64-K half.  Register budget: 168 per
@@ -77,7 +80,12 @@ struct alignas(8) Ctrl {
 constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
 constexpr size_t kL1SmemBytes = 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes;
-constexpr size_t kL2SmemBytes = 1024 + (size_t)kL2Stages * kL2StageBytes + kCtrlBytes;
+// L2 output staging: per epilogue warp 32 rows x 64 BF16 columns (one TMA
+// store box, 128-byte swizzled), written twice per tile.
+constexpr uint32_t kL2OutBytes = 32 * 128;
+constexpr size_t kL2SmemBytes =
+    1024 + (size_t)kL2Stages * kL2StageBytes + (size_t)kL2EpiWarps * kL2OutBytes + kCtrlBytes;
+static_assert(kL2SmemBytes <= 232448, "L2 shared memory");
 
 // Common prologue: barriers, TMEM allocation.  Returns the TMEM base.
 __device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages, int tbufs,
@@ -364,11 +372,12 @@ __global__ void __launch_bounds__(kL1Threads, 1)
 // ============================================================================
 __global__ void __launch_bounds__(kL2Threads, 1)
     l2_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w2,
-              const L2Params p) {
+              const __grid_constant__ CUtensorMap tm_out, const L2Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL2Stages * kL2StageBytes);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL2Stages * kL2StageBytes +
+                                          kL2EpiWarps * kL2OutBytes);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
@@ -457,6 +466,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = q * 32 + (int)lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+        const uint32_t out_stage = base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes;
         const int HB = p.H / 128;                // 128-row weight scale blocks
         int kt = 0;
         bool ok = true;
@@ -466,10 +476,9 @@ __global__ void __launch_bounds__(kL2Threads, 1)
             const bool cols_ok = cb < HB;
             const bool valid = lrow < t.rows && cols_ok;
             const bool warp_on = q * 32 < t.rows && cols_ok;
-            const int row = t.row0 + lrow;
             const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
             // the row's two 64-K activation scales of 128-K block kb: sfa[kb]
-            const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)row * (p.I / 64));
+            const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)(t.row0 + lrow) * (p.I / 64));
 
             float2 acc[64];
 #pragma unroll
@@ -506,14 +515,41 @@ __global__ void __launch_bounds__(kL2Threads, 1)
                         release_tbuf(ctrl, b, lane);
                 }
             }
-            if (!ok || !valid) continue;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + cb * 128);
+            if (!ok || !warp_on) continue;
+            if (q * 32 + 32 <= t.rows) {
+                // all 32 rows of the warp valid: two 32 x 64 boxes through shared
+                // memory and the copy engine (whole 128-byte row pieces)
 #pragma unroll
-            for (int v = 0; v < 16; ++v)
-                dst[v] = make_uint4(bf16x2(acc[4 * v].x, acc[4 * v].y), bf16x2(acc[4 * v + 1].x, acc[4 * v + 1].y),
-                                    bf16x2(acc[4 * v + 2].x, acc[4 * v + 2].y),
-                                    bf16x2(acc[4 * v + 3].x, acc[4 * v + 3].y));
+                for (int k = 0; k < 2; ++k) {
+                    if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
+                    __syncwarp();
+                    const uint32_t rowp = out_stage + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int i = 32 * k + 4 * c;
+                        st_shared_v4(rowp + ((c ^ (lane & 7)) << 4),
+                                     bf16x2(acc[i].x, acc[i].y), bf16x2(acc[i + 1].x, acc[i + 1].y),
+                                     bf16x2(acc[i + 2].x, acc[i + 2].y), bf16x2(acc[i + 3].x, acc[i + 3].y));
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_out, cb * 128 + 64 * k, t.row0 + q * 32, out_stage);
+                        tma_store_commit();
+                    }
+                }
+            } else if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)(t.row0 + lrow) * p.H + cb * 128);
+#pragma unroll
+                for (int v = 0; v < 16; ++v)
+                    dst[v] = make_uint4(bf16x2(acc[4 * v].x, acc[4 * v].y),
+                                        bf16x2(acc[4 * v + 1].x, acc[4 * v + 1].y),
+                                        bf16x2(acc[4 * v + 2].x, acc[4 * v + 2].y),
+                                        bf16x2(acc[4 * v + 3].x, acc[4 * v + 3].y));
+            }
         }
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
     }
     gemm_teardown(tmem, warp);
 }
@@ -544,14 +580,14 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, i
     }
 }
 
-void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
-               cudaStream_t s) {
+void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
+               int num_sms, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
         cudaFuncSetAttribute(l2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
         configured = true;
     }
-    l2_kernel<<<num_sms, kL2Threads, kL2SmemBytes, s>>>(tm_a, tm_w2, p);
+    l2_kernel<<<num_sms, kL2Threads, kL2SmemBytes, s>>>(tm_a, tm_w2, tm_out, p);
 }
 
 }  // namespace moe

@@ -76,8 +76,9 @@ struct L2Params {
     int *err;
     int H, I, E, Pmax;
 };
-void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p, int num_sms,
-               cudaStream_t s);
+// tm_out: l2_out [Pmax, H] BF16 with 32-row x 64-column boxes (128-byte swizzle).
+void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
+               int num_sms, cudaStream_t s);
 
 // FP4-weight configuration: both GEMMs with UE8M0 block scales applied by the
 // tensor core (moe_gemm_fp4.cu).
