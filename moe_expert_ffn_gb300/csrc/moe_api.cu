@@ -175,7 +175,7 @@ struct moe_ctx {
     bool weights_ready;
     int last_T;
     CUtensorMap tm_w1, tm_w2;
-    CUtensorMap tm_l2out;   // l2_out [Pmax, H] BF16, 32-row x 64-column boxes (FP8 L2 epilogue stores)
+    CUtensorMap tm_l2out;   // l2_out [Pmax, H] BF16, 32-row x 64-column boxes (L2 epilogue stores)
     CUtensorMap tm_w1h;     // FP8 W1i as K panels, 128 rows x 2 panels per box (CTA-pair L1)
     CUtensorMap tm_pool3;   // the pool the same way
     AMaps tm_l2a, tm_pool;
@@ -229,9 +229,8 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
                    : make_map(&c->tm_w1, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 256) &&
                          make_map_panels(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 2) &&
                          make_map_panels(&c->tm_pool3, c->ws + L.pool, H, Pm, L.pool_pitch, 128, 2) &&
-                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256) &&
-                         make_map(&c->tm_l2out, c->ws + L.l2_out, H, Pm, H * 2, 64, 32,
-                                  CU_TENSOR_MAP_DATA_TYPE_UINT16));
+                         make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256)) &&
+              make_map(&c->tm_l2out, c->ws + L.l2_out, H, Pm, H * 2, 64, 32, CU_TENSOR_MAP_DATA_TYPE_UINT16);
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
              make_map(&c->tm_pool.box[i], c->ws + L.pool, H, Pm, L.pool_pitch, 128, 32u << i);
@@ -381,7 +380,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
         if (ev) cudaEventRecord(ev[2], s);
         f.a_sf = f.l2_sf;
         f.b_sf = c->wt_at<uint8_t>(L.w2_sf);
-        launch_fp4_l2(c->tm_l2a, c->tm_w2, f, c->num_sms, s);
+        launch_fp4_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, f, c->num_sms, s);
         if (ev) cudaEventRecord(ev[3], s);
         launch_combine(f.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);
         if (ev) cudaEventRecord(ev[4], s);

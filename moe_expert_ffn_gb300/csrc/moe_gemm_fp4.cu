@@ -75,7 +75,16 @@ struct alignas(8) Ctrl {
 };
 constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl");
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kCtrlBytes;
+// L2 output staging: per epilogue warp 32 rows x 64 BF16 columns (one TMA
+// store box, 128-byte swizzled).  L1 has none: its scale writers re-read the
+// tile's scale rows from the L1 cache every stage, and every 16 KB taken from
+// it for shared memory showed (L1 2.3x slower with it).
+constexpr uint32_t kOutBytes = 32 * 128;
+template <bool kL1>
+constexpr uint32_t out_stage_bytes() { return kL1 ? 0u : (uint32_t)kNumEpiWarps * kOutBytes; }
+template <bool kL1>
+constexpr size_t smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + out_stage_bytes<kL1>() + kCtrlBytes; }
+static_assert(smem_bytes<false>() <= 232448, "shared memory");
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t *p) {
     return __ldg(reinterpret_cast<const uint32_t *>(p));
@@ -95,11 +104,12 @@ __device__ __forceinline__ int ue8m0_exponent(float amax) {
 template <bool kL1, bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_b,
-                    const Fp4Params p) {
+                    const __grid_constant__ CUtensorMap tm_out, const Fp4Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kStages * kStageBytes);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kStages * kStageBytes +
+                                          out_stage_bytes<kL1>());
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
@@ -286,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int lrow = q * 32 + (int)lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t out_stage = base + kStages * kStageBytes + (warp - kEpiWarp0) * kOutBytes;
         int tc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
@@ -386,6 +397,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     *reinterpret_cast<uint16_t *>(p.l2_sf + (size_t)row * (p.I / 32) + 2 * cb) =
                         static_cast<uint16_t>(codes);
+                } else if (cb * 128 < p.H && q * 32 + 32 <= t.rows) {
+                    // all 32 rows of the warp valid: two 32 x 64 boxes through
+                    // shared memory and the copy engine (whole 128-byte row pieces)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
+                        __syncwarp();
+                        const uint32_t rowp = out_stage + lane * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int i = 64 * k + 8 * c;
+                            st_shared_v4(rowp + ((c ^ (lane & 7)) << 4), bf16x2(acc[i], acc[i + 1]),
+                                         bf16x2(acc[i + 2], acc[i + 3]), bf16x2(acc[i + 4], acc[i + 5]),
+                                         bf16x2(acc[i + 6], acc[i + 7]));
+                        }
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_out, cb * 128 + 64 * k, t.row0 + q * 32, out_stage);
+                            tma_store_commit();
+                        }
+                    }
                 } else if (cb * 128 < p.H) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)row * p.H + cb * 128);
 #pragma unroll
@@ -397,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (!kL1) {
+            if (lane == 0) tma_store_wait_all();
+            __syncwarp();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -407,33 +444,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kL1, bool kFast, bool kGatherA>
-void launch_t(const AMaps &tm_a, const CUtensorMap &tm_b, const Fp4Params &p, int num_sms,
-              cudaStream_t s) {
+void launch_t(const AMaps &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_out, const Fp4Params &p,
+              int num_sms, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
         cudaFuncSetAttribute(fp4_gemm_kernel<kL1, kFast, kGatherA>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kL1>());
         configured = true;
     }
-    fp4_gemm_kernel<kL1, kFast, kGatherA><<<num_sms, kThreads, kSmemBytes, s>>>(tm_a, tm_b, p);
+    fp4_gemm_kernel<kL1, kFast, kGatherA><<<num_sms, kThreads, smem_bytes<kL1>(), s>>>(tm_a, tm_b, tm_out, p);
 }
 
 }  // namespace
 
 void launch_fp4_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
                    int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+    // (the output map is not used by L1; its codes leave by plain stores)
     if (fast_math) {
-        if (gather_a) launch_t<true, true, true>(tm_a, tm_w1, p, num_sms, s);
-        else launch_t<true, true, false>(tm_a, tm_w1, p, num_sms, s);
+        if (gather_a) launch_t<true, true, true>(tm_a, tm_w1, tm_w1, p, num_sms, s);
+        else launch_t<true, true, false>(tm_a, tm_w1, tm_w1, p, num_sms, s);
     } else {
-        if (gather_a) launch_t<true, false, true>(tm_a, tm_w1, p, num_sms, s);
-        else launch_t<true, false, false>(tm_a, tm_w1, p, num_sms, s);
+        if (gather_a) launch_t<true, false, true>(tm_a, tm_w1, tm_w1, p, num_sms, s);
+        else launch_t<true, false, false>(tm_a, tm_w1, tm_w1, p, num_sms, s);
     }
 }
 
-void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
-                   cudaStream_t s) {
-    launch_t<false, false, false>(tm_a, tm_w2, p, num_sms, s);
+void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const Fp4Params &p,
+                   int num_sms, cudaStream_t s) {
+    launch_t<false, false, false>(tm_a, tm_w2, tm_out, p, num_sms, s);
 }
 
 }  // namespace moe

@@ -96,8 +96,9 @@ struct Fp4Params {
 };
 void launch_fp4_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const Fp4Params &p,
                    int fast_math, bool gather_a, int num_sms, cudaStream_t s);
-void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const Fp4Params &p, int num_sms,
-                   cudaStream_t s);
+// tm_out: l2_out [Pmax, H] BF16 with 32-row x 64-column boxes (128-byte swizzle).
+void launch_fp4_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const Fp4Params &p,
+                   int num_sms, cudaStream_t s);
 
 // FP4 weight transform: W1 packed rows and their UE8M0 scale rows interleaved
 // like the FP8 rows (row bytes given), W2 copied by the caller.
