@@ -42,6 +42,8 @@ SMALL = [
     moe_synth.custom(T=200, H=512, I=384, E=6, k=4, seed=31, name="ragged"),
     moe_synth.custom(T=300, H=256, I=256, E=3, k=2, seed=32, name="nmajor"),
     moe_synth.custom(T=50, H=384, I=128, E=40, k=3, seed=33, name="sparse"),
+    # full 32-row groups next to the half-empty last column block (H % 256 == 128)
+    moe_synth.custom(T=300, H=384, I=256, E=3, k=2, seed=34, name="halfblock"),
 ]
 
 
