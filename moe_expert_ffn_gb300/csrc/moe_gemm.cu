@@ -68,11 +68,19 @@ constexpr uint32_t kL2BBytes = kL2BN * kBK;
 constexpr uint32_t kL2StageBytes = kL2ABytes + kL2BBytes;
 static_assert(kL1TBufs * kL1BN <= (int)kTmemCols && kL2TBufs * kL2BN <= (int)kTmemCols, "TMEM");
 
-struct alignas(8) Ctrl {
+// The producer decodes every tile for its copies; it hands the decoded tile
+// to the epilogue through a small ring (a decode is three dependent global
+// loads, about 1.3 k cycles at a tile start otherwise).
+constexpr int kInfoSlots = 4;
+
+struct alignas(16) Ctrl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t tfull[kMaxTBufs];
     uint64_t tempty[kMaxTBufs];
+    uint64_t info_full[kInfoSlots];
+    uint64_t info_empty[kInfoSlots];
+    int4 info[kInfoSlots];   // e, row0, rows, nb
     uint32_t tmem_base;
     int abort;
 };
@@ -99,6 +107,10 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages,
             mbar_init(smem_u32(&ctrl->tfull[b]), 1);
             mbar_init(smem_u32(&ctrl->tempty[b]), epi_warps);
         }
+        for (int i = 0; i < kInfoSlots; ++i) {
+            mbar_init(smem_u32(&ctrl->info_full[i]), 1);
+            mbar_init(smem_u32(&ctrl->info_empty[i]), epi_warps);
+        }
         ctrl->abort = 0;
         fence_mbar_init();
     }
@@ -119,6 +131,31 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem, int warp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Producer side of the tile ring: publish tile number tc (one thread).
+__device__ __forceinline__ bool put_tile(Ctrl *ctrl, int tc, const Tile &t, volatile int *abort_flag, int *err) {
+    const int i = tc % kInfoSlots;
+    if (!mbar_wait(smem_u32(&ctrl->info_empty[i]), ((tc / kInfoSlots) & 1) ^ 1, abort_flag, err)) return false;
+    ctrl->info[i] = make_int4(t.e, t.row0, t.rows, t.nb);
+    mbar_arrive(smem_u32(&ctrl->info_full[i]));   // release: the slot's contents come first
+    return true;
+}
+
+// Epilogue side: read tile number tc and free its slot (every epilogue warp).
+__device__ __forceinline__ bool get_tile(Ctrl *ctrl, int tc, Tile &t, uint32_t lane, volatile int *abort_flag,
+                                         int *err) {
+    const int i = tc % kInfoSlots;
+    if (!mbar_wait(smem_u32(&ctrl->info_full[i]), (tc / kInfoSlots) & 1, abort_flag, err)) return false;
+    const volatile int *v = reinterpret_cast<const volatile int *>(&ctrl->info[i]);
+    t.e = v[0];
+    t.row0 = v[1];
+    t.rows = v[2];
+    t.nb = v[3];
+    t.nmb = 0;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctrl->info_empty[i]));
+    return true;
 }
 
 // Release TMEM buffer b to the MMA warp (one arrival per epilogue warp).
@@ -199,10 +236,16 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         const uint64_t pol_shared = policy_evict_normal();
         const uint64_t pol_x = policy_evict_last();
         const bool stall = test_stall(p.err, kStallL1);
-        int it = 0;
+        int it = 0, tc = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
             const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            bool put_ok = true;
+            if (lane == 0) put_ok = put_tile(ctrl, tc, t, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
+                ok = false;
+                break;
+            }
             const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
             int tok[4] = {0, 0, 0, 0};
             if (kGatherA) {
@@ -279,10 +322,14 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = q * 32 + (int)lane;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-        int kt = 0;
+        int kt = 0, tc = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
+            Tile t;
+            if (!get_tile(ctrl, tc, t, lane, abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
             const bool valid = lrow < t.rows;
             const bool warp_on = q * 32 < t.rows;
             const int row = t.row0 + lrow;
@@ -399,10 +446,14 @@ __global__ void __launch_bounds__(kL2Threads, 1)
             const uint64_t pol_shared = policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
             const bool stall = test_stall(p.err, kStallL2);
-            int it = 0;
+            int it = 0, tc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
                 const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+                if (!put_tile(ctrl, tc, t, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
                 const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
                 const int wrow = t.e * p.H + t.nb * kL2BN;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -468,10 +519,14 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const uint32_t out_stage = base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes;
         const int HB = p.H / 128;                // 128-row weight scale blocks
-        int kt = 0;
+        int kt = 0, tc = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
+            Tile t;
+            if (!get_tile(ctrl, tc, t, lane, abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
             const int cb = t.nb * 2 + h;         // this warp's 128-column block of H
             const bool cols_ok = cb < HB;
             const bool valid = lrow < t.rows && cols_ok;
