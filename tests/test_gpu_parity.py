@@ -153,6 +153,28 @@ def test_epilogue_options_match_oracle(m, orc, variant, fast, clamp, monkeypatch
     print(f"{variant} fast={fast} clamp={clamp}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
 
 
+@pytest.mark.parametrize("variant", ["single", "pairs", "fp4"])
+def test_fast_math_within_half_percent_of_expf(m, variant, monkeypatch):
+    """The __expf SwiGLU against the expf one on the same inputs (MegaMoE SM90
+    Implementation Design (Final), §21 Phase 4, step 4.4: the fast path within
+    0.5% of the exact one): normalised L2 difference of y below 5e-3, and the
+    L2-activation codes of the two runs mostly equal."""
+    wfmt = 1 if variant == "fp4" else 0
+    monkeypatch.setenv("MOE_L1_PAIR", "1" if variant == "pairs" else "0")
+    wl = moe_synth.custom(T=300, H=512, I=256, E=8, k=2, seed=82, wfmt=wfmt, name="fastexp")
+    inp = moe_synth.make_inputs(wl)
+    la, _, ya = _run(m, wl, inp, wfmt=wfmt, fast_math=False)
+    qa, sa, _ = la.get_intermediates(wl.T)
+    lb, _, yb = _run(m, wl, inp, wfmt=wfmt, fast_math=True)
+    qb, sb, _ = lb.get_intermediates(wl.T)
+    ya, yb = ya.float(), yb.float()
+    rel = float((yb - ya).norm() / ya.norm())
+    assert rel < 5e-3, rel
+    diff = float((qa != qb).float().mean())
+    assert diff < 0.02, diff
+    print(f"{variant}: fast vs expf rel L2 {rel:.2e}, activation codes differing {diff:.2%}")
+
+
 def test_zero_tokens_and_inactive_slots(m, orc):
     wl = moe_synth.custom(T=40, H=256, I=128, E=8, k=3, seed=35)
     inp = moe_synth.make_inputs(wl)
