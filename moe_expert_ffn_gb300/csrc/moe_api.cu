@@ -26,7 +26,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Layout {
     size_t pool_pitch, acts_pitch, w1_pitch, w2_pitch;   // bytes per row
     // workspace
-    size_t err, count, offset, mb_prefix, mblk_expert, mb2_prefix, mblk2_expert, gather, pair_pool;
+    size_t err, count, offset, mb_prefix, mblk_expert, mb2_prefix, mblk2_expert, gather, pair_pool, ready;
     size_t pool, l2_acts, l2_sf, l2_out;
     size_t st_x, st_xsf, st_idx, st_w, st_y;
     size_t ws_total;
@@ -74,6 +74,7 @@ Layout make_layout(const moe_config *c) {
     L.mblk_expert = take(4 * MBmax, 256);
     L.mb2_prefix = take(4 * (E + 1), 256);
     L.mblk2_expert = take(4 * (Pm / (2 * kBM) + E + 1), 256);
+    L.ready = take(4 * MBmax, 256);   // M-block arrival counters of the one-launch GEMM pair
     L.gather = take(4 * Pm, 256);
     L.pair_pool = take(4 * Pm, 256);
     L.pool = take(Pm * L.pool_pitch, kAlign);
@@ -181,6 +182,7 @@ struct moe_ctx {
     AMaps tm_l2a, tm_pool;
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     int l1_pair_mode;       // 0 auto, 1 CTA pairs, 2 single CTAs
+    bool fused;             // both FP8 GEMMs in one cooperative launch (MOE_FUSED=1)
     int test_hook[2];       // armed timeout test for the next forward: {limit us, stall target}
     bool test_armed;
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
@@ -247,6 +249,10 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     // L1 on CTA pairs: MOE_L1_PAIR=1|0 overrides the automatic choice
     c->l1_pair_mode = 0;
     if (const char *m = getenv("MOE_L1_PAIR")) c->l1_pair_mode = (m[0] == '1') ? 1 : 2;
+    // both FP8 GEMMs in one launch, L2 tiles waiting per M block on L1's
+    // arrival counters: MOE_FUSED=1 (off by default)
+    const char *fz = getenv("MOE_FUSED");
+    c->fused = fz && fz[0] == '1';
     // zero the error word
     if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * 4) != cudaSuccess) {
         free(c);
@@ -412,14 +418,6 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     // CTA pairs only on request for now (MOE_L1_PAIR=1): single CTAs are
     // faster end to end on every measured workload
     const bool pair = c->l1_pair_mode == 1 && H % 256 == 0;
-    if (pair) {
-        if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_pool3, c->tm_w1h, p1, g.fast_math, gather_a,
-                           c->num_sms, s) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    } else {
-        launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
-    }
-    if (ev) cudaEventRecord(ev[2], s);
 
     L2Params p2;
     p2.offset = o.offset;
@@ -433,7 +431,29 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     p2.I = I;
     p2.E = E;
     p2.Pmax = Pm;
-    launch_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, p2, c->num_sms, s);
+
+    bool fused_done = false;
+    if (c->fused && !pair) {
+        // one launch for both GEMMs; without room for every CTA at once it
+        // does not launch and the two kernels below run instead
+        int *ready = c->w<int>(L.ready);
+        const size_t ready_bytes = 4 * ((size_t)Pm / kBM + E + 1);
+        if (cudaMemsetAsync(ready, 0, ready_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+        fused_done = launch_fused(gather_a ? tm_x : c->tm_pool, c->tm_w1, c->tm_l2a, c->tm_w2, c->tm_l2out, p1, p2,
+                                  ready, g.fast_math, gather_a, c->num_sms, s) == cudaSuccess;
+        if (!fused_done) (void)cudaGetLastError();
+    }
+    if (!fused_done) {
+        if (pair) {
+            if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_pool3, c->tm_w1h, p1, g.fast_math, gather_a,
+                               c->num_sms, s) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        } else {
+            launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
+        }
+    }
+    if (ev) cudaEventRecord(ev[2], s);
+    if (!fused_done) launch_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, p2, c->num_sms, s);
     if (ev) cudaEventRecord(ev[3], s);
 
     launch_combine(p2.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);

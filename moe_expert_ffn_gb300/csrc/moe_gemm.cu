@@ -200,174 +200,205 @@ __device__ __forceinline__ float acc_at(const float2 (&acc)[64], int i) {
 }
 
 // ============================================================================
-// L1: gate/up GEMM + SwiGLU * w + per-64 FP8 requantisation
+// Warp roles.  Each role walks its CTA's tiles of one GEMM; the running
+// counters live in a Pipe so that one launch can run the L1 tiles and then
+// the L2 tiles through the same stage ring, accumulators and tile ring.
 // ============================================================================
+struct Pipe {
+    int it = 0;      // pipeline stages (producer, MMA issuer)
+    int kt = 0;      // accumulator uses (MMA issuer, epilogue)
+    int tc = 0;      // tiles (tile ring)
+    bool ok = true;
+};
+
+struct Role {
+    Ctrl *ctrl;
+    uint32_t base;   // stage ring
+    uint32_t tmem;
+    volatile int *abort_flag;
+    uint32_t lane;
+    int warp;
+};
+
+// M-block readiness between the GEMMs of one launch: every L1 epilogue warp
+// adds one to its tile's M-block counter after its stores; an L2 tile waits
+// until the counter holds all of that block's L1 tiles (column blocks x
+// epilogue warps).  Bounded like the barrier waits.
+__device__ __forceinline__ void signal_ready(int *ready, int mbi, uint32_t lane) {
+    fence_acq_rel_gpu();   // this lane's stores before the warp's release
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(ready + mbi, 1);
+}
+
+__device__ __forceinline__ bool wait_ready(const int *ready, int mbi, int target, volatile int *abort_flag,
+                                           int *err) {
+    if (ld_acquire_gpu(ready + mbi) >= target) return true;
+    const int lim_us = reinterpret_cast<volatile int *>(err)[1];
+    const uint64_t limit = lim_us > 0 ? 1000ull * (uint64_t)lim_us : kWaitTimeoutNs;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(256);
+        if (ld_acquire_gpu(ready + mbi) >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- L1 roles
 // kGatherA: A rows gathered from x by token with tile::gather4 (tm_a = x,
 // boxes one row high); otherwise A is the pool of gathered rows written by
 // the dispatch step (tm_a = pool, 128-row boxes).
-template <bool kFast, bool kGatherA>
-__global__ void __launch_bounds__(kL1Threads, 1)
-    l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
-              const L1Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = align1024(raw);
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL1Stages * kL1StageBytes);
-    const int warp = threadIdx.x >> 5;
-    const uint32_t lane = threadIdx.x & 31;
-
-    const int NB = p.I / 128;   // 256-row blocks of the interleaved 2I rows
-    const int KB = p.H / kBK;
+template <bool kGatherA>
+__device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
+                                           const Role &r, Pipe &st) {
+    const int NB = p.I / 128, KB = p.H / kBK;
     const int total = __ldg(p.mb_prefix + p.E) * NB;
-
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_a.box[0]);
-        tma_prefetch_desc(&tm_a.box[2]);
-        tma_prefetch_desc(&tm_w1);
-    }
-    const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs, kL1EpiWarps);
-    volatile int *abort_flag = &ctrl->abort;
-
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        // weights of an expert with one M block are read once (evict first);
-        // with several M blocks the tile is shared by neighbouring CTAs
-        const uint64_t pol_once = policy_evict_first();
-        const uint64_t pol_shared = policy_evict_normal();
-        const uint64_t pol_x = policy_evict_last();
-        const bool stall = test_stall(p.err, kStallL1);
-        int it = 0, tc = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
-            bool put_ok = true;
-            if (lane == 0) put_ok = put_tile(ctrl, tc, t, abort_flag, p.err);
-            if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
-                ok = false;
+    const uint32_t lane = r.lane;
+    Ctrl *ctrl = r.ctrl;
+    // weights of an expert with one M block are read once (evict first);
+    // with several M blocks the tile is shared by neighbouring CTAs
+    const uint64_t pol_once = policy_evict_first();
+    const uint64_t pol_shared = policy_evict_normal();
+    const uint64_t pol_x = policy_evict_last();
+    const bool stall = test_stall(p.err, kStallL1);
+    const int it0 = st.it;   // this GEMM's first stage
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+        const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        bool put_ok = true;
+        if (lane == 0) put_ok = put_tile(ctrl, st.tc, t, r.abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
+            st.ok = false;
+            break;
+        }
+        const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
+        int tok[4] = {0, 0, 0, 0};
+        if (kGatherA) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = (int)lane * 4 + i;
+                tok[i] = rr < t.rows ? __ldg(p.gather + t.row0 + rr) / p.k : 0;
+            }
+        }
+        const int wrow = t.e * 2 * p.I + t.nb * kL1BN;
+        // gather4: only the requests that carry valid rows; the other smem
+        // rows keep stale bytes, which reach only masked accumulator rows
+        const int n_g4 = (t.rows + 3) >> 2;
+        const int abox = a_box_index(t.rows);
+        const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : (32u << abox) * kBK) + kL1BBytes;
+        for (int kb = 0; kb < KB; ++kb, ++st.it) {
+            const int s = st.it % kL1Stages;
+            const uint32_t ph = (st.it / kL1Stages) & 1;
+            if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, r.abort_flag, p.err)) {
+                st.ok = false;
                 break;
             }
-            const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
-            int tok[4] = {0, 0, 0, 0};
+            if (stall && st.it == it0) continue;   // timeout-path test: never fill the first stage
+            const uint32_t full = smem_u32(&ctrl->full[s]);
+            if (lane == 0) mbar_arrive_expect_tx(full, tx);
+            __syncwarp();
             if (kGatherA) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = (int)lane * 4 + i;
-                    tok[i] = r < t.rows ? __ldg(p.gather + t.row0 + r) / p.k : 0;
-                }
+                if ((int)lane < n_g4)
+                    tma_gather4(r.base + s * kL1StageBytes + lane * 512, &tm_a.box[0], kb * kBK, tok[0], tok[1],
+                                tok[2], tok[3], full, pol_x);
+            } else if (lane == 0) {
+                tma_load_2d(r.base + s * kL1StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_x);
             }
-            const int wrow = t.e * 2 * p.I + t.nb * kL1BN;
-            // gather4: only the requests that carry valid rows; the other smem
-            // rows keep stale bytes, which reach only masked accumulator rows
-            const int n_g4 = (t.rows + 3) >> 2;
-            const int abox = a_box_index(t.rows);
-            const uint32_t tx = (kGatherA ? (uint32_t)n_g4 * 4 * kBK : (32u << abox) * kBK) + kL1BBytes;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % kL1Stages;
-                const uint32_t ph = (it / kL1Stages) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                if (stall && it == 0) continue;   // timeout-path test: never fill stage 0
-                const uint32_t full = smem_u32(&ctrl->full[s]);
-                if (lane == 0) mbar_arrive_expect_tx(full, tx);
-                __syncwarp();
-                if (kGatherA) {
-                    if ((int)lane < n_g4)
-                        tma_gather4(base + s * kL1StageBytes + lane * 512, &tm_a.box[0], kb * kBK, tok[0],
-                                    tok[1], tok[2], tok[3], full, pol_x);
-                } else if (lane == 0) {
-                    tma_load_2d(base + s * kL1StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_x);
-                }
-                if (lane == 0)
-                    tma_load_2d(base + s * kL1StageBytes + kL1ABytes, &tm_w1, kb * kBK, wrow, full,
-                                pol_w);
-            }
+            if (lane == 0)
+                tma_load_2d(r.base + s * kL1StageBytes + kL1ABytes, &tm_w1, kb * kBK, wrow, full, pol_w);
         }
-        if (!ok) drain_producer(ctrl, it, kL1Stages, p.err);
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
-        int it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % kL1Stages;
-                const uint32_t ph = (it / kL1Stages) & 1;
-                const int b = it % kL1TBufs;
-                const uint32_t tph = (it / kL1TBufs) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
-                    !mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t ad = sw128_kmajor_desc(base + s * kL1StageBytes);
-                    const uint64_t bd = sw128_kmajor_desc(base + s * kL1StageBytes + kL1ABytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk)
-                        umma_e4m3(tmem + b * kL1BN, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0);
-                    umma_commit(smem_u32(&ctrl->empty[s]));
-                    umma_commit(smem_u32(&ctrl->tfull[b]));
-                }
-                __syncwarp();
-            }
-        }
-        if (!ok && it > 0)
-            drain_wait(smem_u32(&ctrl->empty[(it - 1) % kL1Stages]), ((it - 1) / kL1Stages) & 1, p.err);
-    } else {
-        // ---------------- epilogue ----------------
-        const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-        const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
-        const int lrow = q * 32 + (int)lane;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-        int kt = 0, tc = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-            Tile t;
-            if (!get_tile(ctrl, tc, t, lane, abort_flag, p.err)) {
-                ok = false;
+    }
+}
+
+__device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe &st) {
+    const int NB = p.I / 128, KB = p.H / kBK;
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    Ctrl *ctrl = r.ctrl;
+    constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++st.it, ++st.kt) {
+            const int s = st.it % kL1Stages;
+            const uint32_t ph = (st.it / kL1Stages) & 1;
+            const int b = st.kt % kL1TBufs;
+            const uint32_t tph = (st.kt / kL1TBufs) & 1;
+            if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, r.abort_flag, p.err) ||
+                !mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, r.abort_flag, p.err)) {
+                st.ok = false;
                 break;
             }
-            const bool valid = lrow < t.rows;
-            const bool warp_on = q * 32 < t.rows;
-            const int row = t.row0 + lrow;
-            const int pair = valid ? __ldg(p.gather + row) : 0;
-            // the pair's top-k weight, needed only by the tail: load it now
-            const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
-            const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
-            const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
-            const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
-
-            float2 acc[64];
+            tc_fence_after();
+            if (r.lane == 0) {
+                const uint64_t ad = sw128_kmajor_desc(r.base + s * kL1StageBytes);
+                const uint64_t bd = sw128_kmajor_desc(r.base + s * kL1StageBytes + kL1ABytes);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-
-            // scale factors prefetched one K block ahead
-            float sa_n = valid ? __ldg(sfa) : 0.0f;
-            float2 sb_n = __ldg(sfb);
-            for (int kb = 0; kb < KB; ++kb, ++kt) {
-                const int b = kt % kL1TBufs;
-                const uint32_t tph = (kt / kL1TBufs) & 1;
-                const float sa = sa_n;
-                const float2 sb = sb_n;
-                if (kb + 1 < KB) {
-                    sa_n = valid ? __ldg(sfa + kb + 1) : 0.0f;
-                    sb_n = __ldg(sfb + kb + 1);
-                }
-                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (warp_on)
-                    promote128(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
-                else
-                    release_tbuf(ctrl, b, lane);
+                for (int kk = 0; kk < kBK / 32; ++kk)
+                    umma_e4m3(r.tmem + b * kL1BN, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0);
+                umma_commit(smem_u32(&ctrl->empty[s]));
+                umma_commit(smem_u32(&ctrl->tfull[b]));
             }
-            if (!ok || !valid) continue;
+            __syncwarp();
+        }
+    }
+}
 
+// kSignal: add this warp's finished tiles to the M-block counters in `ready`.
+template <bool kFast, bool kSignal>
+__device__ __forceinline__ void l1_epilogue(const L1Params &p, const Role &r, Pipe &st, int *ready) {
+    const int NB = p.I / 128, KB = p.H / kBK;
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const uint32_t lane = r.lane;
+    Ctrl *ctrl = r.ctrl;
+    const int q = r.warp & 3;                  // TMEM lane quadrant this warp may access
+    const int h = (r.warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
+    const int lrow = q * 32 + (int)lane;
+    const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+        Tile t;
+        if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
+            st.ok = false;
+            break;
+        }
+        const bool valid = lrow < t.rows;
+        const bool warp_on = q * 32 < t.rows;
+        const int row = t.row0 + lrow;
+        const int pair = valid ? __ldg(p.gather + row) : 0;
+        // the pair's top-k weight, needed only by the tail: load it now
+        const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
+        const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
+        const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
+        const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
+
+        float2 acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+
+        // scale factors prefetched one K block ahead
+        float sa_n = valid ? __ldg(sfa) : 0.0f;
+        float2 sb_n = __ldg(sfb);
+        for (int kb = 0; kb < KB; ++kb, ++st.kt) {
+            const int b = st.kt % kL1TBufs;
+            const uint32_t tph = (st.kt / kL1TBufs) & 1;
+            const float sa = sa_n;
+            const float2 sb = sb_n;
+            if (kb + 1 < KB) {
+                sa_n = valid ? __ldg(sfa + kb + 1) : 0.0f;
+                sb_n = __ldg(sfb + kb + 1);
+            }
+            if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, r.abort_flag, p.err)) {
+                st.ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (warp_on)
+                promote128(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
+            else
+                release_tbuf(ctrl, b, lane);
+        }
+        if (!st.ok) break;
+        if (valid) {
             // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
             const float clampv = p.clamp;
             float amax = 0.0f;
@@ -410,13 +441,248 @@ __global__ void __launch_bounds__(kL1Threads, 1)
                 dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             p.l2_sf[(size_t)row * (p.I / 64) + jb] = sf;
         }
+        if (kSignal) signal_ready(ready, tile / NB, lane);
+    }
+}
+
+// ---------------------------------------------------------------- L2 roles
+// ready (nullable): wait until the tile's M block counter reaches `target`
+// before copying its activation rows.
+__device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap &tm_w2, const L2Params &p,
+                                           const Role &r, Pipe &st, const int *ready, int target) {
+    const int NB = (p.H + kL2BN - 1) / kL2BN;   // the last block may be half empty (H % 256 == 128)
+    const int KB = p.I / kBK;
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    Ctrl *ctrl = r.ctrl;
+    const uint64_t pol_once = policy_evict_first();
+    const uint64_t pol_shared = policy_evict_normal();
+    const uint64_t pol_a = policy_evict_last();
+    const bool stall = test_stall(p.err, kStallL2);
+    const int it0 = st.it;   // this GEMM's first stage
+    int last_mbi = -1;
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+        const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        if (!put_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
+            st.ok = false;
+            break;
+        }
+        if (ready && tile / NB != last_mbi) {
+            last_mbi = tile / NB;
+            if (!wait_ready(ready, last_mbi, target, r.abort_flag, p.err)) {
+                st.ok = false;
+                break;
+            }
+            fence_proxy_async_global();   // the rows the acquire made visible, for the copy engine
+        }
+        const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
+        const int wrow = t.e * p.H + t.nb * kL2BN;
+        for (int kb = 0; kb < KB; ++kb, ++st.it) {
+            const int s = st.it % kL2Stages;
+            const uint32_t ph = (st.it / kL2Stages) & 1;
+            if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, r.abort_flag, p.err)) {
+                st.ok = false;
+                break;
+            }
+            if (stall && st.it == it0) continue;   // timeout-path test: never fill the first stage
+            const uint32_t full = smem_u32(&ctrl->full[s]);
+            const int abox = a_box_index(t.rows);
+            mbar_arrive_expect_tx(full, (32u << abox) * kBK + kL2BBytes);
+            tma_load_2d(r.base + s * kL2StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_a);
+            tma_load_2d(r.base + s * kL2StageBytes + kL2ABytes, &tm_w2, kb * kBK, wrow, full, pol_w);
+        }
+    }
+}
+
+// Each 128-K stage is two 64-K halves, each into its own accumulator.
+__device__ __forceinline__ void l2_issue(const L2Params &p, const Role &r, Pipe &st) {
+    const int NB = (p.H + kL2BN - 1) / kL2BN;
+    const int KB = p.I / kBK;
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    Ctrl *ctrl = r.ctrl;
+    constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL2BN);
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x) {
+        for (int kb = 0; st.ok && kb < KB; ++kb, ++st.it) {
+            const int s = st.it % kL2Stages;
+            const uint32_t ph = (st.it / kL2Stages) & 1;
+            if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, r.abort_flag, p.err)) {
+                st.ok = false;
+                break;
+            }
+            const uint64_t ad = sw128_kmajor_desc(r.base + s * kL2StageBytes);
+            const uint64_t bd = sw128_kmajor_desc(r.base + s * kL2StageBytes + kL2ABytes);
+#pragma unroll
+            for (int half = 0; half < 2; ++half, ++st.kt) {
+                const int b = st.kt % kL2TBufs;
+                const uint32_t tph = (st.kt / kL2TBufs) & 1;
+                if (!mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, r.abort_flag, p.err)) {
+                    st.ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (r.lane == 0) {
+                    umma_e4m3(r.tmem + b * kL2BN, ad + 4 * half, bd + 4 * half, idesc, 0);
+                    umma_e4m3(r.tmem + b * kL2BN, ad + 4 * half + 2, bd + 4 * half + 2, idesc, 1);
+                    umma_commit(smem_u32(&ctrl->tfull[b]));
+                }
+                __syncwarp();
+            }
+            if (st.ok && r.lane == 0) umma_commit(smem_u32(&ctrl->empty[s]));
+            __syncwarp();
+        }
+    }
+}
+
+// kAcquire: the L1 outputs of this launch are read after the tile's M block
+// is ready (an acquire by lane 0, then L2-coherent loads of the scales).
+template <bool kAcquire>
+__device__ __forceinline__ float2 load_sa(const float2 *p) {
+    if (kAcquire) return ld_cg_f32x2(p);
+    return __ldg(p);
+}
+
+template <bool kAcquire>
+__device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2Params &p, const Role &r, Pipe &st,
+                                            uint32_t out_stage, const int *ready, int target) {
+    const int NB = (p.H + kL2BN - 1) / kL2BN;
+    const int KB = p.I / kBK;
+    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const uint32_t lane = r.lane;
+    Ctrl *ctrl = r.ctrl;
+    const int q = r.warp & 3;
+    const int h = (r.warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
+    const int lrow = q * 32 + (int)lane;
+    const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+    const int HB = p.H / 128;                  // 128-row weight scale blocks
+    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+        Tile t;
+        if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
+            st.ok = false;
+            break;
+        }
+        if (kAcquire) {
+            bool rd = true;
+            if (lane == 0) rd = wait_ready(ready, tile / NB, target, r.abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, rd, 0)) {
+                st.ok = false;
+                break;
+            }
+            __syncwarp();   // lane 0's acquire before every lane's loads
+        }
+        const int cb = t.nb * 2 + h;           // this warp's 128-column block of H
+        const bool cols_ok = cb < HB;
+        const bool valid = lrow < t.rows && cols_ok;
+        const bool warp_on = q * 32 < t.rows && cols_ok;
+        const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
+        // the row's two 64-K activation scales of 128-K block kb: sfa[kb]
+        const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)(t.row0 + lrow) * (p.I / 64));
+
+        float2 acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+
+        // scales prefetched two 128-K blocks ahead (a far L2 hit takes
+        // longer than one block's promotion)
+        const float2 z2 = make_float2(0.0f, 0.0f);
+        float2 sa0 = valid ? load_sa<kAcquire>(sfa) : z2;
+        float2 sa1 = (valid && KB > 1) ? load_sa<kAcquire>(sfa + 1) : z2;
+        float sb0 = __ldg(sfb);
+        float sb1 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
+        for (int kb = 0; st.ok && kb < KB; ++kb) {
+            const float2 sa = sa0;
+            const float sb = sb0;
+            sa0 = sa1;
+            sb0 = sb1;
+            if (kb + 2 < KB) {
+                if (valid) sa1 = load_sa<kAcquire>(sfa + kb + 2);
+                sb1 = __ldg(sfb + kb + 2);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half, ++st.kt) {
+                const float sc = (half ? sa.y : sa.x) * sb;
+                const int b = st.kt % kL2TBufs;
+                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (st.kt / kL2TBufs) & 1, r.abort_flag, p.err)) {
+                    st.ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (warp_on)
+                    promote128(acc, t_lane + b * kL2BN, sc, sc, ctrl, b, lane);
+                else
+                    release_tbuf(ctrl, b, lane);
+            }
+        }
+        if (!st.ok || !warp_on) continue;
+        if (q * 32 + 32 <= t.rows) {
+            // all 32 rows of the warp valid: two 32 x 64 boxes through shared
+            // memory and the copy engine (whole 128-byte row pieces)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
+                __syncwarp();
+                const uint32_t rowp = out_stage + lane * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int i = 32 * k + 4 * c;
+                    st_shared_v4(rowp + ((c ^ (lane & 7)) << 4), bf16x2(acc[i].x, acc[i].y),
+                                 bf16x2(acc[i + 1].x, acc[i + 1].y), bf16x2(acc[i + 2].x, acc[i + 2].y),
+                                 bf16x2(acc[i + 3].x, acc[i + 3].y));
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tm_out, cb * 128 + 64 * k, t.row0 + q * 32, out_stage);
+                    tma_store_commit();
+                }
+            }
+        } else if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)(t.row0 + lrow) * p.H + cb * 128);
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+                dst[v] = make_uint4(bf16x2(acc[4 * v].x, acc[4 * v].y), bf16x2(acc[4 * v + 1].x, acc[4 * v + 1].y),
+                                    bf16x2(acc[4 * v + 2].x, acc[4 * v + 2].y),
+                                    bf16x2(acc[4 * v + 3].x, acc[4 * v + 3].y));
+        }
+    }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
+}
+
+// ============================================================================
+// Kernels
+// ============================================================================
+// L1: gate/up GEMM + SwiGLU * w + per-64 FP8 requantisation.
+template <bool kFast, bool kGatherA>
+__global__ void __launch_bounds__(kL1Threads, 1)
+    l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
+              const L1Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align1024(raw);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL1Stages * kL1StageBytes);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a.box[0]);
+        tma_prefetch_desc(&tm_a.box[2]);
+        tma_prefetch_desc(&tm_w1);
+    }
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs, kL1EpiWarps);
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    Pipe st;
+    if (warp == 0) {
+        l1_produce<kGatherA>(tm_a, tm_w1, p, r, st);
+        if (!st.ok) drain_producer(ctrl, st.it, kL1Stages, p.err);
+    } else if (warp == 1) {
+        l1_issue(p, r, st);
+        if (!st.ok && st.kt > 0)
+            drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL1TBufs]), ((st.kt - 1) / kL1TBufs) & 1, p.err);
+    } else {
+        l1_epilogue<kFast, false>(p, r, st, nullptr);
     }
     gemm_teardown(tmem, warp);
 }
 
-// ============================================================================
-// L2: down GEMM with per-64 activation scales, BF16 output in pool order
-// ============================================================================
+// L2: down GEMM with per-64 activation scales, BF16 output in pool order.
 __global__ void __launch_bounds__(kL2Threads, 1)
     l2_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w2,
               const __grid_constant__ CUtensorMap tm_out, const L2Params p) {
@@ -427,184 +693,76 @@ __global__ void __launch_bounds__(kL2Threads, 1)
                                           kL2EpiWarps * kL2OutBytes);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
-
-    const int NB = (p.H + kL2BN - 1) / kL2BN;   // the last block may be half empty (H % 256 == 128)
-    const int KB = p.I / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
-
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_a.box[0]);
         tma_prefetch_desc(&tm_a.box[2]);
         tma_prefetch_desc(&tm_w2);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
-    volatile int *abort_flag = &ctrl->abort;
-
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    Pipe st;
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol_once = policy_evict_first();
-            const uint64_t pol_shared = policy_evict_normal();
-            const uint64_t pol_a = policy_evict_last();
-            const bool stall = test_stall(p.err, kStallL2);
-            int it = 0, tc = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-                const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
-                if (!put_tile(ctrl, tc, t, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
-                const int wrow = t.e * p.H + t.nb * kL2BN;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kL2Stages;
-                    const uint32_t ph = (it / kL2Stages) & 1;
-                    if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    if (stall && it == 0) continue;   // timeout-path test: never fill stage 0
-                    const uint32_t full = smem_u32(&ctrl->full[s]);
-                    const int abox = a_box_index(t.rows);
-                    mbar_arrive_expect_tx(full, (32u << abox) * kBK + kL2BBytes);
-                    tma_load_2d(base + s * kL2StageBytes, &tm_a.box[abox], kb * kBK, t.row0, full, pol_a);
-                    tma_load_2d(base + s * kL2StageBytes + kL2ABytes, &tm_w2, kb * kBK, wrow, full,
-                                pol_w);
-                }
-            }
-            if (!ok) drain_producer(ctrl, it, kL2Stages, p.err);
+            l2_produce(tm_a, tm_w2, p, r, st, nullptr, 0);
+            if (!st.ok) drain_producer(ctrl, st.it, kL2Stages, p.err);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // Each 128-K stage is two 64-K halves, each into its own accumulator.
-        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL2BN);
-        int it = 0, kt = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            for (int kb = 0; ok && kb < KB; ++kb, ++it) {
-                const int s = it % kL2Stages;
-                const uint32_t ph = (it / kL2Stages) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t ad = sw128_kmajor_desc(base + s * kL2StageBytes);
-                const uint64_t bd = sw128_kmajor_desc(base + s * kL2StageBytes + kL2ABytes);
-#pragma unroll
-                for (int half = 0; half < 2; ++half, ++kt) {
-                    const int b = kt % kL2TBufs;
-                    const uint32_t tph = (kt / kL2TBufs) & 1;
-                    if (!mbar_wait(smem_u32(&ctrl->tempty[b]), tph ^ 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        umma_e4m3(tmem + b * kL2BN, ad + 4 * half, bd + 4 * half, idesc, 0);
-                        umma_e4m3(tmem + b * kL2BN, ad + 4 * half + 2, bd + 4 * half + 2, idesc, 1);
-                        umma_commit(smem_u32(&ctrl->tfull[b]));
-                    }
-                    __syncwarp();
-                }
-                if (ok && lane == 0) umma_commit(smem_u32(&ctrl->empty[s]));
-                __syncwarp();
-            }
-        }
-        if (!ok && kt > 0)
-            drain_wait(smem_u32(&ctrl->tfull[(kt - 1) % kL2TBufs]), ((kt - 1) / kL2TBufs) & 1, p.err);
+        l2_issue(p, r, st);
+        if (!st.ok && st.kt > 0)
+            drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL2TBufs]), ((st.kt - 1) / kL2TBufs) & 1, p.err);
     } else {
-        const int q = warp & 3;
-        const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
-        const int lrow = q * 32 + (int)lane;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-        const uint32_t out_stage = base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes;
-        const int HB = p.H / 128;                // 128-row weight scale blocks
-        int kt = 0, tc = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-            Tile t;
-            if (!get_tile(ctrl, tc, t, lane, abort_flag, p.err)) {
-                ok = false;
-                break;
-            }
-            const int cb = t.nb * 2 + h;         // this warp's 128-column block of H
-            const bool cols_ok = cb < HB;
-            const bool valid = lrow < t.rows && cols_ok;
-            const bool warp_on = q * 32 < t.rows && cols_ok;
-            const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
-            // the row's two 64-K activation scales of 128-K block kb: sfa[kb]
-            const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)(t.row0 + lrow) * (p.I / 64));
+        l2_epilogue<false>(tm_out, p, r, st, base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes,
+                           nullptr, 0);
+    }
+    gemm_teardown(tmem, warp);
+}
 
-            float2 acc[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-
-            // scales prefetched two 128-K blocks ahead (a far L2 hit takes
-            // longer than one block's promotion)
-            const float2 z2 = make_float2(0.0f, 0.0f);
-            float2 sa0 = valid ? __ldg(sfa) : z2;
-            float2 sa1 = (valid && KB > 1) ? __ldg(sfa + 1) : z2;
-            float sb0 = __ldg(sfb);
-            float sb1 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
-            for (int kb = 0; ok && kb < KB; ++kb) {
-                const float2 sa = sa0;
-                const float sb = sb0;
-                sa0 = sa1;
-                sb0 = sb1;
-                if (kb + 2 < KB) {
-                    if (valid) sa1 = __ldg(sfa + kb + 2);
-                    sb1 = __ldg(sfb + kb + 2);
-                }
-#pragma unroll
-                for (int half = 0; half < 2; ++half, ++kt) {
-                    const float sc = (half ? sa.y : sa.x) * sb;
-                    const int b = kt % kL2TBufs;
-                    if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (kt / kL2TBufs) & 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (warp_on)
-                        promote128(acc, t_lane + b * kL2BN, sc, sc, ctrl, b, lane);
-                    else
-                        release_tbuf(ctrl, b, lane);
-                }
-            }
-            if (!ok || !warp_on) continue;
-            if (q * 32 + 32 <= t.rows) {
-                // all 32 rows of the warp valid: two 32 x 64 boxes through shared
-                // memory and the copy engine (whole 128-byte row pieces)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
-                    __syncwarp();
-                    const uint32_t rowp = out_stage + lane * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int i = 32 * k + 4 * c;
-                        st_shared_v4(rowp + ((c ^ (lane & 7)) << 4),
-                                     bf16x2(acc[i].x, acc[i].y), bf16x2(acc[i + 1].x, acc[i + 1].y),
-                                     bf16x2(acc[i + 2].x, acc[i + 2].y), bf16x2(acc[i + 3].x, acc[i + 3].y));
-                    }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tm_out, cb * 128 + 64 * k, t.row0 + q * 32, out_stage);
-                        tma_store_commit();
-                    }
-                }
-            } else if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_out + (size_t)(t.row0 + lrow) * p.H + cb * 128);
-#pragma unroll
-                for (int v = 0; v < 16; ++v)
-                    dst[v] = make_uint4(bf16x2(acc[4 * v].x, acc[4 * v].y),
-                                        bf16x2(acc[4 * v + 1].x, acc[4 * v + 1].y),
-                                        bf16x2(acc[4 * v + 2].x, acc[4 * v + 2].y),
-                                        bf16x2(acc[4 * v + 3].x, acc[4 * v + 3].y));
-            }
-        }
-        if (lane == 0) tma_store_wait_all();
+// Both GEMMs in one persistent launch (every CTA resident: a cooperative
+// launch).  Each CTA runs its L1 tiles and then its L2 tiles through the same
+// stage ring, accumulators and tile ring; an L2 tile starts once the L1 tiles
+// of its M block (on any CTA) have stored their outputs, so L2 work fills the
+// SMs that finish L1 early (the pages' fused pipeline with arrival counters,
+// design §3.3, on one GPU).
+template <bool kFast, bool kGatherA>
+__global__ void __launch_bounds__(kL2Threads, 1)
+    fused_kernel(const __grid_constant__ AMaps tm_a1, const __grid_constant__ CUtensorMap tm_w1,
+                 const __grid_constant__ AMaps tm_a2, const __grid_constant__ CUtensorMap tm_w2,
+                 const __grid_constant__ CUtensorMap tm_out, const L1Params p1, const L2Params p2, int *ready) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align1024(raw);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL2Stages * kL2StageBytes +
+                                          kL2EpiWarps * kL2OutBytes);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a1.box[0]);
+        tma_prefetch_desc(&tm_w1);
+        tma_prefetch_desc(&tm_a2.box[2]);
+        tma_prefetch_desc(&tm_w2);
+    }
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    const int target = (p1.I / 128) * kL1EpiWarps;   // L1 tile-warps per M block
+    Pipe st;
+    if (warp == 0) {
+        l1_produce<kGatherA>(tm_a1, tm_w1, p1, r, st);
+        if (lane == 0 && st.ok) l2_produce(tm_a2, tm_w2, p2, r, st, ready, target);
+        st.ok = __shfl_sync(0xffffffffu, st.ok, 0);
+        st.it = __shfl_sync(0xffffffffu, st.it, 0);
+        if (!st.ok && lane == 0) drain_producer(ctrl, st.it, kL2Stages, p1.err);
         __syncwarp();
+    } else if (warp == 1) {
+        l1_issue(p1, r, st);
+        if (st.ok) l2_issue(p2, r, st);
+        if (!st.ok && st.kt > 0)
+            drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL2TBufs]), ((st.kt - 1) / kL2TBufs) & 1, p1.err);
+    } else {
+        l1_epilogue<kFast, true>(p1, r, st, ready);
+        if (st.ok)
+            l2_epilogue<true>(tm_out, p2, r, st,
+                              base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready, target);
     }
     gemm_teardown(tmem, warp);
 }
@@ -633,6 +791,40 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, i
         if (gather_a) launch_l1_t<false, true>(tm_a, tm_w1, p, num_sms, s);
         else launch_l1_t<false, false>(tm_a, tm_w1, p, num_sms, s);
     }
+}
+
+template <bool kFast, bool kGatherA>
+static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2,
+                                  const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1,
+                                  const L2Params &p2, int *ready, int num_sms, cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(fused_kernel<kFast, kGatherA>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: L2 tiles wait on other CTAs' L1 tiles
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kL2Threads);
+    cfg.dynamicSmemBytes = kL2SmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_kernel<kFast, kGatherA>, tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready);
+}
+
+cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2, const CUtensorMap &tm_w2,
+                         const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2, int *ready,
+                         int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+    if (fast_math)
+        return gather_a ? launch_fused_t<true, true>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
+                        : launch_fused_t<true, false>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
+    return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
+                    : launch_fused_t<false, false>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
 }
 
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,

@@ -76,6 +76,13 @@ struct L2Params {
     int *err;
     int H, I, E, Pmax;
 };
+// Both FP8 GEMMs in one cooperative launch (L2 tiles wait per M block on
+// the L1 tiles' arrival counters in `ready`, [M blocks] zeroed beforehand).
+// Fails without launching when not every CTA can be resident.
+cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2, const CUtensorMap &tm_w2,
+                         const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2, int *ready,
+                         int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+
 // tm_out: l2_out [Pmax, H] BF16 with 32-row x 64-column boxes (128-byte swizzle).
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
                int num_sms, cudaStream_t s);

@@ -30,8 +30,12 @@ def m():
     return mod
 
 
+@pytest.mark.parametrize("fused", ["0", "1"], ids=["two_launches", "one_launch"])
 @pytest.mark.parametrize("which", [1, 2], ids=["l1", "l2"])
-def test_timeout_is_reported_and_context_recovers(m, which):
+def test_timeout_is_reported_and_context_recovers(m, which, fused, monkeypatch):
+    # one_launch: both GEMMs in one kernel, where L2 tiles of other CTAs also
+    # wait (bounded) for the M block the withheld stage belongs to
+    monkeypatch.setenv("MOE_FUSED", fused)
     wl = moe_synth.custom(T=96, H=512, I=256, E=4, k=2, seed=71)
     inp = to_dev(moe_synth.make_inputs(wl), DEV)
     layer = new_layer(m, wl, DEV)

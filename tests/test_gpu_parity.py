@@ -136,6 +136,46 @@ def test_l1_cta_pairs_match_oracle(m, orc, wl, a_mode, monkeypatch):
     print(f"{wl.name}/pairs/{a_mode}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
 
 
+# Both FP8 GEMMs in one cooperative launch (MOE_FUSED=1): the same
+# arithmetic as the two launches, so y must be bit-identical to theirs; and
+# within tolerance of the oracle.  Small cases plus an expert mix where many
+# M blocks finish their L1 tiles at different times.
+FUSED_CASES = SMALL + [moe_synth.custom(T=600, H=512, I=256, E=8, k=2, seed=38, name="fused_counts")]
+
+
+@pytest.mark.parametrize("wl", FUSED_CASES, ids=lambda w: w.name)
+def test_fused_launch_matches_two_launches(m, orc, wl, monkeypatch):
+    inp = moe_synth.make_inputs(wl)
+    if wl.name == "fused_counts":
+        inp["topk_idx"] = _crafted_counts(wl.T, wl.k, wl.E, [1, 127, 128, 129, 255, 256, 257, 47], wl.seed)
+    monkeypatch.setenv("MOE_FUSED", "0")
+    _, _, y2 = _run(m, wl, inp)
+    monkeypatch.setenv("MOE_FUSED", "1")
+    _, _, y1 = _run(m, wl, inp)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref = bf16_bits_to_float(orc.forward(inp))
+    rel, mx = assert_y_close(y1, ref, f"{wl.name}/fused")
+    print(f"{wl.name}/fused: bit-identical to two launches, rel L2 {rel:.2e}")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_fused_launch_full_size(m, name, monkeypatch):
+    """Full sizes in the bench's launch configuration: the one-launch y equals
+    the two-launch y bit for bit."""
+    wl = moe_synth.WORKLOADS[name]
+    inp = moe_synth.make_inputs(wl, device=DEV)
+    ys = []
+    for fused in ("0", "1"):
+        monkeypatch.setenv("MOE_FUSED", fused)
+        layer = new_layer(m, wl, DEV)
+        layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+        ys.append(layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"]).clone())
+        torch.cuda.synchronize()
+        assert layer.device_status() == m.MOE_OK
+        del layer
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+
+
 @pytest.mark.parametrize("clamp", [float("inf"), 1.0], ids=["noclamp", "clamp1"])
 @pytest.mark.parametrize("fast", [0, 1], ids=["expf", "fastexp"])
 @pytest.mark.parametrize("variant", ["single", "pairs", "fp4"])
