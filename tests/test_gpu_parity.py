@@ -285,6 +285,47 @@ def test_one_expert_takes_everything(m, orc):
     assert_y_close(y[torch.from_numpy(sel).long().to(DEV)], ref, "one expert")
 
 
+# Degenerate shapes: one token, top-1 with a single expert (the layer is then
+# a dense FFN of that expert), E = 1, and a layer created for more tokens than
+# the call passes (the pool and tile tables sized for max_tokens).
+EDGE = [
+    moe_synth.custom(T=1, H=256, I=128, E=8, k=2, seed=91, name="one_token"),
+    moe_synth.custom(T=1, H=256, I=128, E=8, k=8, seed=92, name="one_token_k8"),
+    moe_synth.custom(T=77, H=384, I=256, E=1, k=1, seed=93, name="single_expert"),
+    moe_synth.custom(T=130, H=256, I=128, E=16, k=1, seed=94, name="top1"),
+]
+
+
+@pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
+@pytest.mark.parametrize("wfmt", [0, 1], ids=["fp8", "fp4"])
+def test_degenerate_shapes_match_oracle(m, orc, wl, wfmt):
+    wl = moe_synth.custom(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, seed=wl.seed, wfmt=wfmt, name=wl.name)
+    inp = moe_synth.make_inputs(wl)
+    layer, g, y = _run(m, wl, inp, wfmt=wfmt)
+    ref = bf16_bits_to_float(orc.forward(inp, wfmt=wfmt))
+    assert_y_close(y, ref, f"{wl.name}/{'fp4' if wfmt else 'fp8'}")
+    counts, offsets, gather = layer.get_dispatch(wl.T)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"], wl.E)
+    assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
+
+
+def test_fewer_tokens_than_capacity(m, orc):
+    """A layer sized for 512 tokens called with 100 and then 512: each call
+    matches the oracle for its own tokens."""
+    big = moe_synth.custom(T=512, H=256, I=256, E=8, k=2, seed=95, name="capacity")
+    inp = moe_synth.make_inputs(big)
+    layer = new_layer(m, big, DEV)
+    g = to_dev(inp, DEV)
+    layer.transform_weights(g["w1"], g["w1_sf"], g["w2"], g["w2_sf"])
+    for T in (100, 512):
+        y = layer.forward(g["x"][:T].contiguous(), g["x_sf"][:T].contiguous(), g["topk_idx"][:T].contiguous(),
+                          g["topk_weights"][:T].contiguous())
+        torch.cuda.synchronize()
+        assert layer.device_status() == m.MOE_OK
+        sub = {n: (t[:T].contiguous() if n in ("x", "x_sf", "topk_idx", "topk_weights") else t) for n, t in inp.items()}
+        assert_y_close(y, bf16_bits_to_float(orc.forward(sub)), f"T={T} of 512")
+
+
 @pytest.mark.parametrize("name", ["decode", "prefill", "wide"])
 def test_full_size_sampled_tokens(m, orc, name):
     wl = moe_synth.WORKLOADS[name]
