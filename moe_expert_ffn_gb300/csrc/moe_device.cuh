@@ -33,12 +33,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -119,23 +113,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tm), "r"(x), "r"(y), "r"(bar), "l"(cache_hint)
         : "memory");
-}
-
-// 3-D box {x, y, z} into shared memory, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
-                                            uint32_t bar, uint64_t cache_hint) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(cache_hint)
-        : "memory");
-}
-
-// Prefetch a 2-D box into L2 (no shared memory, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(x),
-                 "r"(y)
-                 : "memory");
 }
 
 // Four rows r0..r3 of a 2-D tensor (box one row high) into four consecutive
