@@ -169,12 +169,10 @@ void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *
 void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
                      cudaStream_t s) {
     const size_t smem = sizeof(int32_t) * (size_t)(kWarps * E + E + 1);
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(int32_t) * (kWarps * 1024 + 1025)));
-        configured = true;
-    }
+    static std::atomic<uint32_t> smem_set{0};
+    if (smem_limit_once(reinterpret_cast<const void *>(dispatch_kernel), sizeof(int32_t) * (kWarps * 1024 + 1025),
+                        smem_set) != cudaSuccess)
+        return;   // the launch below would fail the same way; the caller's error check reports it
     dispatch_kernel<<<1, kThreads, smem, s>>>(topk_idx, T, k, E, o);
 }
 

@@ -773,12 +773,8 @@ __global__ void __launch_bounds__(kL2Threads, 1)
 template <bool kFast, bool kGatherA>
 static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
                         int num_sms, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(l1_kernel<kFast, kGatherA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kL1SmemBytes);
-        configured = true;
-    }
+    static std::atomic<uint32_t> smem_set{0};
+    smem_limit_once(reinterpret_cast<const void *>(l1_kernel<kFast, kGatherA>), kL1SmemBytes, smem_set);
     l1_kernel<kFast, kGatherA><<<num_sms, kL1Threads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
 }
 
@@ -797,13 +793,10 @@ template <bool kFast, bool kGatherA>
 static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2,
                                   const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1,
                                   const L2Params &p2, int *ready, int num_sms, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(fused_kernel<kFast, kGatherA>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint32_t> smem_set{0};
+    const cudaError_t e =
+        smem_limit_once(reinterpret_cast<const void *>(fused_kernel<kFast, kGatherA>), kL2SmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: L2 tiles wait on other CTAs' L1 tiles
@@ -829,11 +822,8 @@ cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMa
 
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
                int num_sms, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(l2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kL2SmemBytes);
-        configured = true;
-    }
+    static std::atomic<uint32_t> smem_set{0};
+    smem_limit_once(reinterpret_cast<const void *>(l2_kernel), kL2SmemBytes, smem_set);
     l2_kernel<<<num_sms, kL2Threads, kL2SmemBytes, s>>>(tm_a, tm_w2, tm_out, p);
 }
 

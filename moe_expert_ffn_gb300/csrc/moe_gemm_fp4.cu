@@ -446,12 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kL1, bool kFast, bool kGatherA>
 void launch_t(const AMaps &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_out, const Fp4Params &p,
               int num_sms, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(fp4_gemm_kernel<kL1, kFast, kGatherA>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kL1>());
-        configured = true;
-    }
+    static std::atomic<uint32_t> smem_set{0};
+    smem_limit_once(reinterpret_cast<const void *>(fp4_gemm_kernel<kL1, kFast, kGatherA>), smem_bytes<kL1>(),
+                    smem_set);
     fp4_gemm_kernel<kL1, kFast, kGatherA><<<num_sms, kThreads, smem_bytes<kL1>(), s>>>(tm_a, tm_b, tm_out, p);
 }
 

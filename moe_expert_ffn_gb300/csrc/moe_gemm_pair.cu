@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kFast, bool kGatherA>
 static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
                                  const L1Params &p, int num_sms, cudaStream_t s) {
-    static int grid = 0;
+    static std::atomic<int> grids[32];   // per device: the resident-pair grid, 0 until computed
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -394,9 +394,13 @@ static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, co
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    int grid = grids[dev & 31].load(std::memory_order_acquire);
     if (!grid) {
-        cudaError_t e = cudaFuncSetAttribute(l1_pair_kernel<kFast, kGatherA>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        static std::atomic<uint32_t> smem_set{0};
+        cudaError_t e = smem_limit_once(reinterpret_cast<const void *>(l1_pair_kernel<kFast, kGatherA>), kSmemBytes,
+                                        smem_set);
         if (e != cudaSuccess) return e;
         // as many pairs as can be resident at once (a persistent grid)
         cfg.gridDim = dim3(num_sms & ~1);
@@ -404,6 +408,7 @@ static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, co
         e = cudaOccupancyMaxActiveClusters(&clusters, l1_pair_kernel<kFast, kGatherA>, &cfg);
         if (e != cudaSuccess || clusters < 1) return e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
         grid = 2 * min(clusters, num_sms / 2);
+        grids[dev & 31].store(grid, std::memory_order_release);
     }
     cfg.gridDim = dim3(grid);
     return cudaLaunchKernelEx(&cfg, l1_pair_kernel<kFast, kGatherA>, tm_a, tm_a3, tm_w1h, p);

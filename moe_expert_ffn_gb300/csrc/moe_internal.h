@@ -6,7 +6,22 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace moe {
+
+// A kernel's dynamic shared-memory limit is an attribute of the function on
+// each device: set it once per device (one bit per device in `done`, so a
+// process that drives several GPUs sets it on each).
+inline cudaError_t smem_limit_once(const void *func, size_t bytes, std::atomic<uint32_t> &done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint32_t bit = 1u << (dev & 31);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 constexpr int kBM = 128;   // pool rows (routed pairs) per M block
 constexpr int kBK = 128;   // K bytes per pipeline stage (one scale block)
