@@ -266,8 +266,18 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
     const uint64_t pol_x = policy_evict_last();
     const bool stall = test_stall(p.err, kStallL1);
     const int it0 = st.it;   // this GEMM's first stage
+    // the next tile is decoded during this one (its dependent loads would
+    // otherwise hold back the copies at every tile start)
+    const int kb_fin = min(1, KB - 1);
+    TilePrefetch pf;
+    if ((int)blockIdx.x < total) {
+        pf.begin(blockIdx.x, NB, p.mblk_expert);
+        pf.finish(p.offset, p.mb_prefix);
+    }
     for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
-        const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        const Tile t = pf.tile(NB);
+        const bool has_next = tile + (int)gridDim.x < total;
+        if (has_next) pf.begin(tile + gridDim.x, NB, p.mblk_expert);
         bool put_ok = true;
         if (lane == 0) put_ok = put_tile(ctrl, st.tc, t, r.abort_flag, p.err);
         if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
@@ -296,6 +306,7 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
                 st.ok = false;
                 break;
             }
+            if (has_next && kb == kb_fin) pf.finish(p.offset, p.mb_prefix);
             if (stall && st.it == it0) continue;   // timeout-path test: never fill the first stage
             const uint32_t full = smem_u32(&ctrl->full[s]);
             if (lane == 0) mbar_arrive_expect_tx(full, tx);
@@ -460,8 +471,17 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
     const bool stall = test_stall(p.err, kStallL2);
     const int it0 = st.it;   // this GEMM's first stage
     int last_mbi = -1;
+    // the next tile is decoded during this one, as in the L1 producer
+    const int kb_fin = min(1, KB - 1);
+    TilePrefetch pf;
+    if ((int)blockIdx.x < total) {
+        pf.begin(blockIdx.x, NB, p.mblk_expert);
+        pf.finish(p.offset, p.mb_prefix);
+    }
     for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
-        const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+        const Tile t = pf.tile(NB);
+        const bool has_next = tile + (int)gridDim.x < total;
+        if (has_next) pf.begin(tile + gridDim.x, NB, p.mblk_expert);
         if (!put_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
             st.ok = false;
             break;
@@ -483,6 +503,7 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
                 st.ok = false;
                 break;
             }
+            if (has_next && kb == kb_fin) pf.finish(p.offset, p.mb_prefix);
             if (stall && st.it == it0) continue;   // timeout-path test: never fill the first stage
             const uint32_t full = smem_u32(&ctrl->full[s]);
             const int abox = a_box_index(t.rows);

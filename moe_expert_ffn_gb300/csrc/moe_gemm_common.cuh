@@ -15,16 +15,8 @@ struct Tile {
 // order, each expert's M blocks x NB column blocks walked N-major when the
 // expert has at least kNMajorMinRows pairs (weight tile reused across
 // consecutive CTAs), M-major otherwise (design §12.2 "Auto N-Major").
-__device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__restrict__ offset,
-                                            const int32_t *__restrict__ mb_prefix,
-                                            const int32_t *__restrict__ mblk_expert) {
+__device__ __forceinline__ Tile make_tile(int tile, int NB, int e, int first, int nmb, int off, int cnt) {
     Tile t;
-    const int mbi = tile / NB;
-    const int e = __ldg(mblk_expert + mbi);
-    const int first = __ldg(mb_prefix + e);
-    const int nmb = __ldg(mb_prefix + e + 1) - first;
-    const int off = __ldg(offset + e);
-    const int cnt = __ldg(offset + e + 1) - off;
     const int local = tile - first * NB;
     int mb, nb;
     if (cnt >= kNMajorMinRows) {
@@ -41,6 +33,37 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__r
     t.nmb = nmb;
     return t;
 }
+
+__device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__restrict__ offset,
+                                            const int32_t *__restrict__ mb_prefix,
+                                            const int32_t *__restrict__ mblk_expert) {
+    const int e = __ldg(mblk_expert + tile / NB);
+    const int first = __ldg(mb_prefix + e);
+    const int nmb = __ldg(mb_prefix + e + 1) - first;
+    const int off = __ldg(offset + e);
+    const int cnt = __ldg(offset + e + 1) - off;
+    return make_tile(tile, NB, e, first, nmb, off, cnt);
+}
+
+// The same decode in two steps, for a producer that must not stall on it:
+// begin() loads the tile's expert, finish() (once that has arrived, a stage
+// or so later) the expert's offsets; tile() then needs no load.
+struct TilePrefetch {
+    int tl, e, first, first1, off, off1;
+    __device__ __forceinline__ void begin(int tile, int NB, const int32_t *mblk_expert) {
+        tl = tile;
+        e = __ldg(mblk_expert + tile / NB);
+    }
+    __device__ __forceinline__ void finish(const int32_t *offset, const int32_t *mb_prefix) {
+        first = __ldg(mb_prefix + e);
+        first1 = __ldg(mb_prefix + e + 1);
+        off = __ldg(offset + e);
+        off1 = __ldg(offset + e + 1);
+    }
+    __device__ __forceinline__ Tile tile(int NB) const {
+        return make_tile(tl, NB, e, first, first1 - first, off, off1 - off);
+    }
+};
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
