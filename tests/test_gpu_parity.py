@@ -44,6 +44,9 @@ SMALL = [
     moe_synth.custom(T=50, H=384, I=128, E=40, k=3, seed=33, name="sparse"),
     # full 32-row groups next to the half-empty last column block (H % 256 == 128)
     moe_synth.custom(T=300, H=384, I=256, E=3, k=2, seed=34, name="halfblock"),
+    # Zipf routing: experts of 3-5 M blocks (N-major walk), of 2 (M-major)
+    # and of one, and an empty one, in one launch
+    moe_synth.custom(T=600, H=256, I=256, E=32, k=4, seed=35, routing="zipf", name="skewed"),
 ]
 
 
@@ -351,6 +354,7 @@ FP4 = [
     moe_synth.custom(T=40, H=256, I=128, E=8, k=2, seed=61, wfmt=1, name="fp4_tiny"),
     moe_synth.custom(T=300, H=512, I=384, E=6, k=3, seed=62, wfmt=1, name="fp4_ragged"),
     moe_synth.custom(T=64, H=384, I=256, E=40, k=4, seed=63, wfmt=1, n_empty=8, name="fp4_sparse"),
+    moe_synth.custom(T=600, H=256, I=128, E=32, k=4, seed=64, wfmt=1, routing="zipf", name="fp4_skewed"),
 ]
 
 
