@@ -238,6 +238,26 @@ def time_oracle(inp, wfmt=0):
     return time.perf_counter() - t0
 
 
+# --------------------------------------------------------------------------- replicas
+def reduce_max(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the slowest replica sets the step time).
+
+    `device` is where the collective's tensor lives: the rank's GPU under
+    NCCL, None (host memory) under gloo."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every replica's tokens over the slowest step."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def run_reference(args, wl, rank, world):
     """The reference arm: the CPU oracle, on a bounded token sample per step."""
     if rank != 0:
@@ -318,10 +338,7 @@ def run_ours(args, wl, rank, world, local_rank):
     stage_ms, nfw = layer.profile_end()
     if layer.device_status() != m.MOE_OK:
         raise RuntimeError("device error in the timed region")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms = reduce_max(ms, world, dev)
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -342,13 +359,9 @@ def run_ours(args, wl, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = t.item()
+        e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
         h2d = hx.numel() + hsf.numel() * 4 + hidx.numel() * 4 + hw.numel() * 4
-        e2e = {"value": world * wl.T / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(world, wl.T, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hy.numel() * 2, "ms_per_step": e_ms}
 
     if rank != 0:
@@ -366,7 +379,7 @@ def run_ours(args, wl, rank, world, local_rank):
     t_roof = max(wm["flops"]["layer"] / tens, wm["bytes"]["layer"] / (peaks["hbm_gbs"] * 1e9))
 
     out = {
-        "metric": METRIC, "value": world * wl.T / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_value(world, wl.T, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 (fp32 accumulate)" if wl.wfmt == 0 else "fp8_e4m3 x fp4_e2m1, ue8m0 block scales (fp32 accumulate)",
