@@ -58,8 +58,9 @@ constexpr uint32_t kL1ABytes = kBM * kBK;
 constexpr uint32_t kL1BBytes = kL1BN * kBK;
 constexpr uint32_t kL1StageBytes = kL1ABytes + kL1BBytes;
 // L2: 128 x 256 tiles, a ring of two 256-column accumulators (one per 64-K
-// half of a stage), 4 stages of 48 KB.  (A K=32 MMA takes about the same
-// time at N=128 as at N=256, so the wide tile doubles the tensor throughput.)
+// half of a stage), 4 stages of 48 KB.  (The wide tile does twice the tensor
+// work per stage hand-off and per token-row copy of a 128 x 128 tile; that
+// tile, with a four-deep ring of 128-column accumulators, measured slower.)
 constexpr int kL2BN = 256;
 constexpr int kL2TBufs = 2;
 constexpr int kL2Stages = 4;
