@@ -350,6 +350,31 @@ def test_full_size_sampled_tokens(m, orc, name):
     assert torch.isfinite(y.float()).all()
 
 
+def test_largest_batch_sampled_tokens(m, orc):
+    """Four times the prefill batch (131072 routed pairs, 1024 M blocks, 16384
+    L1 and 28672 L2 tiles): dispatch maps bit-exact and sampled tokens,
+    including the first and the last, within the layer tolerance."""
+    wl = moe_synth.custom(T=16384, H=7168, I=2048, E=256, k=8, seed=41, name="largest")
+    inp = moe_synth.make_inputs(wl, device=DEV)
+    layer = new_layer(m, wl, DEV)
+    layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    rng = np.random.default_rng(11)
+    tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=4, replace=False)])).astype(np.int32)
+    sub = sub_inputs(inp, tokens)   # the oracle needs only the experts these tokens use
+    del inp["w1"], inp["w2"]
+    y = layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    counts, offsets, gather = layer.get_dispatch(wl.T)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
+    assert int(oo[-1]) == wl.T * wl.k
+    assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
+    ref = bf16_bits_to_float(orc.forward(sub))
+    rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, "largest")
+    print(f"largest: sampled tokens {tokens.tolist()} rel L2 {rel:.2e} max/rms {mx:.2e}")
+    assert torch.isfinite(y.float()).all()
+
+
 FP4 = [
     moe_synth.custom(T=40, H=256, I=128, E=8, k=2, seed=61, wfmt=1, name="fp4_tiny"),
     moe_synth.custom(T=300, H=512, I=384, E=6, k=3, seed=62, wfmt=1, name="fp4_ragged"),
