@@ -516,6 +516,12 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
 }
 
 // Each 128-K stage is two 64-K halves, each into its own accumulator.
+// kOneCommit: the second half's MMAs are the stage's last, so the stage's
+// empty commit also tells the epilogue that half is done, and the half needs
+// no commit of its own (one commit fewer per stage on the issuing thread).
+// The one-launch GEMM pair keeps both, because its epilogue counts uses
+// across both GEMMs.
+template <bool kOneCommit>
 __device__ __forceinline__ void l2_issue(const L2Params &p, const Role &r, Pipe &st) {
     const int NB = (p.H + kL2BN - 1) / kL2BN;
     const int KB = p.I / kBK;
@@ -544,7 +550,7 @@ __device__ __forceinline__ void l2_issue(const L2Params &p, const Role &r, Pipe 
                 if (r.lane == 0) {
                     umma_e4m3(r.tmem + b * kL2BN, ad + 4 * half, bd + 4 * half, idesc, 0);
                     umma_e4m3(r.tmem + b * kL2BN, ad + 4 * half + 2, bd + 4 * half + 2, idesc, 1);
-                    umma_commit(smem_u32(&ctrl->tfull[b]));
+                    if (!(kOneCommit && half == 1)) umma_commit(smem_u32(&ctrl->tfull[b]));
                 }
                 __syncwarp();
             }
@@ -562,7 +568,7 @@ __device__ __forceinline__ float2 load_sa(const float2 *p) {
     return __ldg(p);
 }
 
-template <bool kAcquire>
+template <bool kAcquire, bool kOneCommit>
 __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2Params &p, const Role &r, Pipe &st,
                                             uint32_t out_stage, const int *ready, int target) {
     const int NB = (p.H + kL2BN - 1) / kL2BN;
@@ -622,7 +628,16 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
             for (int half = 0; half < 2; ++half, ++st.kt) {
                 const float sc = (half ? sa.y : sa.x) * sb;
                 const int b = st.kt % kL2TBufs;
-                if (!mbar_wait(smem_u32(&ctrl->tfull[b]), (st.kt / kL2TBufs) & 1, r.abort_flag, p.err)) {
+                // kOneCommit: the second half waits for its stage's empty
+                // barrier (use kt of a launch that starts at use 0 is half
+                // kt % 2 of stage kt / 2)
+                const int js = st.kt >> 1;
+                const bool got = (kOneCommit && half == 1)
+                                     ? mbar_wait(smem_u32(&ctrl->empty[js % kL2Stages]), (js / kL2Stages) & 1,
+                                                 r.abort_flag, p.err)
+                                     : mbar_wait(smem_u32(&ctrl->tfull[b]), (st.kt / kL2TBufs) & 1, r.abort_flag,
+                                                 p.err);
+                if (!got) {
                     st.ok = false;
                     break;
                 }
@@ -730,11 +745,16 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        l2_issue(p, r, st);
-        if (!st.ok && st.kt > 0)
-            drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL2TBufs]), ((st.kt - 1) / kL2TBufs) & 1, p.err);
+        l2_issue<true>(p, r, st);
+        if (!st.ok && st.kt > 0) {   // the last committed use: a first half (tfull) or a stage (empty)
+            const int u = st.kt - 1;
+            if (u & 1)
+                drain_wait(smem_u32(&ctrl->empty[(u >> 1) % kL2Stages]), ((u >> 1) / kL2Stages) & 1, p.err);
+            else
+                drain_wait(smem_u32(&ctrl->tfull[u % kL2TBufs]), (u / kL2TBufs) & 1, p.err);
+        }
     } else {
-        l2_epilogue<false>(tm_out, p, r, st, base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes,
+        l2_epilogue<false, true>(tm_out, p, r, st, base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes,
                            nullptr, 0);
     }
     gemm_teardown(tmem, warp);
@@ -777,13 +797,13 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         __syncwarp();
     } else if (warp == 1) {
         l1_issue(p1, r, st);
-        if (st.ok) l2_issue(p2, r, st);
+        if (st.ok) l2_issue<false>(p2, r, st);
         if (!st.ok && st.kt > 0)
             drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL2TBufs]), ((st.kt - 1) / kL2TBufs) & 1, p1.err);
     } else {
         l1_epilogue<kFast, true>(p1, r, st, ready);
         if (st.ok)
-            l2_epilogue<true>(tm_out, p2, r, st,
+            l2_epilogue<true, false>(tm_out, p2, r, st,
                               base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready, target);
     }
     gemm_teardown(tmem, warp);
