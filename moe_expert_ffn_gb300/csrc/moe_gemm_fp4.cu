@@ -29,7 +29,10 @@
 //              reads the scale of row r from TMEM lane 32*(m/32) + r%32 (m =
 //              the output row being computed), column base + r/32, so each lane
 //              quadrant holds a full copy: lane 32q + j, column base + c = row
-//              32c + j;
+//              32c + j.  They take a stage slot when the MMA's commit frees it
+//              (the producer's empty barrier) and arrive on the slot's full
+//              barrier next to the producer, so the MMA issuer waits once per
+//              stage and commits once;
 //   warps 6-9  epilogue, one per TMEM lane quadrant: each thread moves the
 //              first 128 of its row's 256 accumulator columns to a TMEM stash,
 //              reads the second 128 into registers and frees the accumulator
@@ -66,8 +69,6 @@ static_assert(kStashCol0 + 128 <= kTmemCols, "TMEM budget");
 struct alignas(8) Ctrl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t sf_full[kStages];
-    uint64_t sf_empty[kStages];
     uint64_t acc_full[kAccs];
     uint64_t acc_empty[kAccs];
     uint32_t tmem_base;
@@ -123,10 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ctrl->full[s]), 1);
+            mbar_init(smem_u32(&ctrl->full[s]), 1 + kNumSfWarps);   // the copies and the scale writers
             mbar_init(smem_u32(&ctrl->empty[s]), 1);
-            mbar_init(smem_u32(&ctrl->sf_full[s]), kNumSfWarps);
-            mbar_init(smem_u32(&ctrl->sf_empty[s]), 1);
         }
         for (int b = 0; b < kAccs; ++b) {
             mbar_init(smem_u32(&ctrl->acc_full[b]), 1);
@@ -207,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err) ||
-                    !mbar_wait(smem_u32(&ctrl->sf_full[s]), ph, abort_flag, p.err)) {
+                if (!mbar_wait(smem_u32(&ctrl->full[s]), ph, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
@@ -222,7 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_mx(tmem + b * kBN, ad + 2 * kk, bd + 2 * kk, idesc_mx_e4m3_e2m1(kBM, kBN, kk),
                                 sfa, sfa + kSfACols, (kb | kk) != 0);
                     umma_commit(smem_u32(&ctrl->empty[s]));
-                    umma_commit(smem_u32(&ctrl->sf_empty[s]));
                     if (kb == KB - 1) umma_commit(smem_u32(&ctrl->acc_full[b]));
                 }
                 __syncwarp();
@@ -272,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) na[c] = ld_u32(arow[c] + kn);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) nbw[c] = ld_u32(brow[c] + kn);
-                if (!mbar_wait(smem_u32(&ctrl->sf_empty[s]), ph ^ 1, abort_flag, p.err)) {
+                if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
@@ -284,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctrl->sf_full[s]));
+                if (lane == 0) mbar_arrive(smem_u32(&ctrl->full[s]));
 #pragma unroll
                 for (int c = 0; c < 4; ++c) wa[c] = na[c];
 #pragma unroll
