@@ -27,6 +27,7 @@ struct Layout {
     size_t pool_pitch, acts_pitch, w1_pitch, w2_pitch;   // bytes per row
     // workspace
     size_t err, count, offset, mb_prefix, mblk_expert, mb2_prefix, mblk2_expert, gather, pair_pool, ready;
+    size_t dcnt;   // per-CTA expert counts of the multi-CTA dispatch
     size_t pool, l2_acts, l2_sf, l2_out;
     size_t st_x, st_xsf, st_idx, st_w, st_y;
     size_t ws_total;
@@ -75,6 +76,7 @@ Layout make_layout(const moe_config *c) {
     L.mb2_prefix = take(4 * (E + 1), 256);
     L.mblk2_expert = take(4 * (Pm / (2 * kBM) + E + 1), 256);
     L.ready = take(4 * MBmax, 256);   // M-block arrival counters of the one-launch GEMM pair
+    L.dcnt = take(4 * (size_t)kDispatchMcMaxCtas * E, 256);
     L.gather = take(4 * Pm, 256);
     L.pair_pool = take(4 * Pm, 256);
     L.pool = take(Pm * L.pool_pitch, kAlign);
@@ -347,7 +349,16 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     o.err = c->w<int>(L.err);
     cudaEvent_t *ev = (c->prof_ev && c->prof_n < c->prof_max) ? c->prof_ev + 5 * c->prof_n++ : nullptr;
     if (ev) cudaEventRecord(ev[0], s);
-    launch_dispatch(topk_idx, T, k, E, o, s);
+    // large batches: the dispatch over several CTAs (one per 1024 pairs, at
+    // most one per SM); the single-CTA kernel if that launch is refused
+    bool dispatched = false;
+    if ((long long)T * k >= kDispatchMcMinPairs) {
+        const int ctas = std::min(std::min(c->num_sms, kDispatchMcMaxCtas), (T * k + 1023) / 1024);
+        dispatched = launch_dispatch_mc(topk_idx, T, k, E, o, c->w<int32_t>(L.dcnt), c->w<int>(L.err) + 3,
+                                        ctas, s) == cudaSuccess;
+        if (!dispatched) (void)cudaGetLastError();
+    }
+    if (!dispatched) launch_dispatch(topk_idx, T, k, E, o, s);
     if (ev) cudaEventRecord(ev[1], s);
 
     // A operand: gather token rows in the L1 producer (tile::gather4) when the

@@ -19,7 +19,8 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 // The device error block (4 ints in the workspace): [0] error bits, [1] wait
 // limit in microseconds for a test of the timeout path (0 = kWaitTimeoutNs),
 // [2] test stall target (kStallL1 / kStallL2: CTA 0's producer in that GEMM
-// withholds the copies of its first stage), [3] unused.
+// withholds the copies of its first stage), [3] the arrival counter of the
+// multi-CTA dispatch's grid-wide barrier.
 constexpr int kStallL1 = 1;
 constexpr int kStallL2 = 2;
 

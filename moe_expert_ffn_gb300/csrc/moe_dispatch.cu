@@ -139,6 +139,134 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// The same dispatch over G CTAs, for large batches (one CTA's 32 warps would
+// walk dozens of 32-pair batches each, one dependent memory round trip after
+// another).  A cooperative launch (every CTA resident).  CTA c takes the
+// pairs [c*chunk, (c+1)*chunk) and runs the per-warp passes of
+// dispatch_kernel on them; between the passes one grid-wide barrier (bounded)
+// separates writing the CTA's per-expert counts from reading every CTA's:
+// each CTA then knows the expert offsets and its own first slot inside each
+// expert, so the stable (token, slot) order holds across CTAs.  CTA 0 writes
+// the per-expert tables.  `bar` is zero before the launch.
+__global__ void __launch_bounds__(kThreads, 1)
+    dispatch_mc_kernel(const int32_t *__restrict__ idx, int T, int k, int E, DispatchOut o,
+                       int32_t *__restrict__ cta_cnt, int *bar) {
+    extern __shared__ int32_t sm[];
+    int32_t *hist = sm;                 // [kWarps][E]: count, then first slot of the warp
+    int32_t *off_s = sm + kWarps * E;   // [E+1]
+    __shared__ int warp_tot[kWarps];
+    __shared__ int tot_a, tot_b, tot_c, bad, go;
+
+    const int P = T * k;
+    const int chunk = (P + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int c0 = min(P, (int)blockIdx.x * chunk), c1 = min(P, c0 + chunk);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) hist[i] = 0;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+
+    const int seg = (c1 - c0 + kWarps - 1) / kWarps;
+    const int p0 = min(c1, c0 + warp * seg), p1 = min(c1, p0 + seg);
+
+    // pass 1: per-warp histogram of this CTA's pairs
+    for (int p = p0 + lane; p < p1; p += 32) {
+        const int e = __ldg(idx + p);
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[warp * E + e], 1);
+        else if (e != -1)
+            bad = 1;
+    }
+    __syncthreads();
+    int cnt = 0;
+    if (threadIdx.x < E) {
+        const int e = threadIdx.x;
+        for (int w = 0; w < kWarps; ++w) {
+            const int h = hist[w * E + e];
+            hist[w * E + e] = cnt;
+            cnt += h;
+        }
+        cta_cnt[(size_t)blockIdx.x * E + e] = cnt;
+        __threadfence();
+    }
+    if (threadIdx.x == 0 && bad) atomicOr(o.err, kErrBadExpert);
+
+    // every CTA's counts written before any is read
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        red_release_gpu_add(bar, 1);
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(bar) < (int)gridDim.x) {
+            __nanosleep(64);
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                atomicOr(o.err, kErrTimeout);
+                ok = false;
+                break;
+            }
+        }
+        go = ok;
+    }
+    __syncthreads();
+    if (!go) return;
+
+    // the expert totals and this CTA's first slot inside each expert
+    int total = 0, before = 0;
+    if (threadIdx.x < E) {
+        for (int c = 0; c < (int)gridDim.x; ++c) {
+            const int v = __ldcg(cta_cnt + (size_t)c * E + threadIdx.x);
+            total += v;
+            if (c < (int)blockIdx.x) before += v;
+        }
+    }
+    const int off = block_exclusive_scan(total, warp_tot, &tot_a);
+    if (threadIdx.x < E) off_s[threadIdx.x] = off + before;
+    if (blockIdx.x == 0) {
+        const int nmb = (total + kBM - 1) / kBM;
+        const int nmb2 = (total + 2 * kBM - 1) / (2 * kBM);
+        const int mbo = block_exclusive_scan(nmb, warp_tot, &tot_b);
+        const int mbo2 = block_exclusive_scan(nmb2, warp_tot, &tot_c);
+        if (threadIdx.x < E) {
+            o.count[threadIdx.x] = total;
+            o.offset[threadIdx.x] = off;
+            o.mb_prefix[threadIdx.x] = mbo;
+            if (o.stats) o.stats[threadIdx.x] += total;
+            for (int b = 0; b < nmb; ++b) o.mblk_expert[mbo + b] = threadIdx.x;
+            if (o.mb2_prefix) {
+                o.mb2_prefix[threadIdx.x] = mbo2;
+                for (int b = 0; b < nmb2; ++b) o.mblk2_expert[mbo2 + b] = threadIdx.x;
+            }
+        }
+        if (threadIdx.x == 0) {
+            o.offset[E] = tot_a;
+            o.mb_prefix[E] = tot_b;
+            if (o.mb2_prefix) o.mb2_prefix[E] = tot_c;
+        }
+    }
+    __syncthreads();
+
+    // pass 2: stable positions, batch by batch in pair order
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = p0; base < p1; base += 32) {
+        const int p = base + lane;
+        const int e = (p < p1) ? __ldg(idx + p) : -1;
+        const bool ok = e >= 0 && e < E;
+        const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1);
+        int rank = 0;
+        if (ok) {
+            rank = __popc(grp & lt_mask);
+            const int pos = off_s[e] + hist[warp * E + e] + rank;
+            o.gather[pos] = p;
+            o.pair_pool[p] = pos;
+        } else if (p < p1) {
+            o.pair_pool[p] = -1;
+        }
+        __syncwarp();
+        if (ok && rank == __popc(grp) - 1) hist[warp * E + e] += __popc(grp);
+        __syncwarp();
+    }
+}
+
 // The pages' "pull into the L1 pool" on one GPU (design §9.2): the FP8 row of
 // the token of every pool row, in dispatch order.  One warp per row.
 __global__ void __launch_bounds__(256)
@@ -174,6 +302,27 @@ void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const Dispatc
                         smem_set) != cudaSuccess)
         return;   // the launch below would fail the same way; the caller's error check reports it
     dispatch_kernel<<<1, kThreads, smem, s>>>(topk_idx, T, k, E, o);
+}
+
+cudaError_t launch_dispatch_mc(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                               int32_t *cta_cnt, int *bar, int ctas, cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * (size_t)(kWarps * E + E + 1);
+    static std::atomic<uint32_t> smem_set{0};
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void *>(dispatch_mc_kernel),
+                                    sizeof(int32_t) * (kWarps * 1024 + 1025), smem_set);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(bar, 0, sizeof(int), s)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // the grid-wide barrier needs every CTA resident
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_mc_kernel, topk_idx, T, k, E, o, cta_cnt, bar);
 }
 
 }  // namespace moe

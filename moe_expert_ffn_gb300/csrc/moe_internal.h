@@ -52,6 +52,15 @@ struct DispatchOut {
 void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
                      cudaStream_t s);
 
+// The same dispatch over `ctas` CTAs of one cooperative launch (large
+// batches): cta_cnt [ctas, E] scratch, bar one int of scratch (zeroed here,
+// in the stream, before the launch).  Fails without launching when not every
+// CTA can be resident.
+constexpr int kDispatchMcMinPairs = 8192;   // smaller batches: one CTA (measured faster at 4096)
+constexpr int kDispatchMcMaxCtas = 256;
+cudaError_t launch_dispatch_mc(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                               int32_t *cta_cnt, int *bar, int ctas, cudaStream_t s);
+
 // L1: x (gathered by pool row) . W1i^T, SwiGLU * w, per-64 FP8 requant.
 struct L1Params {
     const int32_t *gather, *offset, *mb_prefix, *mblk_expert;

@@ -47,6 +47,8 @@ SMALL = [
     # Zipf routing: experts of 3-5 M blocks (N-major walk), of 2 (M-major)
     # and of one, and an empty one, in one launch
     moe_synth.custom(T=600, H=256, I=256, E=32, k=4, seed=35, routing="zipf", name="skewed"),
+    # 8192 pairs: the dispatch runs over 8 CTAs, hot experts spanning them
+    moe_synth.custom(T=2048, H=256, I=128, E=64, k=4, seed=36, routing="zipf", name="multi_cta_dispatch"),
 ]
 
 
