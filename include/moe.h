@@ -55,7 +55,7 @@ extern "C" {
 
 #define MOE_OK 0
 #define MOE_ERR_INVALID_ARG (-1)    /* null pointer, bad size, misaligned buffer */
-#define MOE_ERR_UNSUPPORTED (-2)    /* shape or format this build does not run */
+#define MOE_ERR_UNSUPPORTED (-2)    /* shape or format this library does not run */
 #define MOE_ERR_CUDA (-3)           /* a CUDA runtime/driver call failed */
 #define MOE_ERR_DEVICE_TIMEOUT (-4) /* a bounded device-side wait gave up */
 #define MOE_ERR_BAD_EXPERT (-5)     /* topk_idx held an id outside [-1, E) */
