@@ -3,7 +3,8 @@
 
 A step is one forward of the whole layer (dispatch -> L1 GEMM + SwiGLU +
 requant -> L2 GEMM -> combine) over one batch of T synthetic tokens of the
-chosen workload (default: decode, T=128 H=7168 I=2048 E=256 k=8).
+chosen workload (default: prefill, T=4096 H=7168 I=2048 E=256 k=8, Zipf-skewed
+routing: the largest configuration of the layer that fits one GPU).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -41,7 +42,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="prefill")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -86,14 +86,30 @@ typedef struct {
                          division is the fast one (<= 2 ulp) either way */
 } moe_config;
 
-/* Bytes of device workspace / transformed-weight storage for `cfg`
- * (0 if `cfg` is invalid). */
+/* Bytes of device workspace for `cfg` (0 if `cfg` is invalid).  The pages
+ * size the layer's one buffer with a call of its own (MegaMoE SM90
+ * Implementation Design (Final), §16.1 "get_symm_buffer_size_for_sm90_mega_moe";
+ * PR357 Green-Context Split MegaMoE code review, §3.1 "Split symmetric
+ * buffer"); on one GPU the symmetric buffer is a plain device buffer holding
+ * the dispatch tables, the token pool, the L2 activations and their scales,
+ * the BF16 pair outputs and the staging of moe_forward_host.  The pages'
+ * token-alignment query (design §16.1 "get_token_alignment_for_sm90_mega_moe")
+ * has no counterpart: any num_tokens in [0, max_tokens] is accepted. */
 MOE_API size_t moe_workspace_bytes(const moe_config *cfg);
+
+/* Bytes of the transformed-weight store for `cfg` (0 if `cfg` is invalid):
+ * what moe_transform_weights writes (design §16.1
+ * "transform_weights_for_mega_moe_sm90", §15; PR357 review §3.2 "Weight
+ * transform"). */
 MOE_API size_t moe_weight_bytes(const moe_config *cfg);
 
-/* Create a context bound to the current CUDA device.  d_workspace and
- * d_weights are caller-owned device buffers of the sizes above (256-byte
- * aligned).  Writes *out on success. */
+/* Create a context bound to the current CUDA device.  The configuration
+ * carries the arguments the pages' entry point takes besides its tensors
+ * (design §16.1 fp8_mega_moe: num_max_tokens_per_rank, num_experts,
+ * num_topk, the (1, 1, 128) recipe, activation_clamp, fast_math), minus the
+ * rank and symmetric-buffer arguments.  d_workspace and d_weights are
+ * caller-owned device buffers of the sizes above (256-byte aligned).  Writes
+ * *out on success. */
 MOE_API int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_weights);
 
 /* Read the canonical weights and write the kernel layout into d_weights
@@ -124,7 +140,8 @@ MOE_API int moe_forward(moe_ctx *ctx, int num_tokens, const void *x, const void 
                 const int32_t *topk_idx, const float *topk_weights, void *y,
                 int32_t *cumulative_expert_counts, void *stream);
 
-/* moe_forward with HOST inputs and output: copies h_x, h_x_sf, h_topk_idx,
+/* moe_forward with HOST inputs and output (the pages define no such call:
+ * their layer reads inputs already in the symmetric buffer): copies h_x, h_x_sf, h_topk_idx,
  * h_topk_weights into the workspace, runs the forward and copies y back to
  * h_y, then synchronises `stream`.  Host buffers may be pageable or pinned
  * (pinned is faster). */
@@ -132,7 +149,8 @@ MOE_API int moe_forward_host(moe_ctx *ctx, int num_tokens, const void *h_x, cons
                      const int32_t *h_topk_idx, const float *h_topk_weights, void *h_y,
                      void *stream);
 
-/* Copy the dispatch result of the last forward (T tokens) into caller device
+/* Test export (the pages define no such call): copy the dispatch result of
+ * the last forward (T tokens) into caller device
  * buffers: counts int32 [E], offsets int32 [E+1] (exclusive prefix of
  * counts), gather int32 [T*k] whose first offsets[E] entries are the pair ids
  * t*k + j of each expert's pairs in (token, slot) order, experts ascending
@@ -140,7 +158,8 @@ MOE_API int moe_forward_host(moe_ctx *ctx, int num_tokens, const void *h_x, cons
 MOE_API int moe_get_dispatch(moe_ctx *ctx, int32_t *counts, int32_t *offsets, int32_t *gather,
                      void *stream);
 
-/* Copy intermediates of the last forward (T tokens; row r belongs to pair
+/* Test export (the pages define no such call): copy intermediates of the
+ * last forward (T tokens; row r belongs to pair
  * gather[r], rows r >= offsets[E] unspecified), P = T*k:
  * l2_acts u8 (E4M3) [P, I], l2_sf = the L2 activation scales (f32 [P, I/64]
  * with FP8 weights, u8 UE8M0 [P, I/32] with FP4 weights),
@@ -172,6 +191,8 @@ MOE_API int moe_get_intermediates(moe_ctx *ctx, void *l2_acts, void *l2_sf, void
  *    MOE_NOALLOC_MAX_EXPERTS, topk outside [1, 32], or a pointer is NULL.
  *  - The first call on a device looks up that array's device address (with
  *    that device current); make this first call before any stream capture.
+ *    The address is kept per device and context: after cudaDeviceReset the
+ *    next call looks it up again in the new context.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    the call clears what must start at zero.  Calls that overlap on the GPU
  *    (two streams, or two host threads) race on it and must not be issued.
@@ -180,7 +201,8 @@ MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tokens, int to
                                  int num_experts, int32_t *counts, int32_t *offsets,
                                  int32_t *gather, void *stream);
 
-/* Per-stage timing of the next `max_forwards` forwards: moe_profile_begin
+/* Measurement plumbing (the pages define no such call).
+ * Per-stage timing of the next `max_forwards` forwards: moe_profile_begin
  * creates CUDA events (no device memory) and every following moe_forward
  * records one event before its dispatch and one after each of its four
  * stages (dispatch, L1 GEMM, L2 GEMM, combine) on its stream.
@@ -192,24 +214,34 @@ MOE_API int moe_profile_end(moe_ctx *ctx, float *stage_ms, int *n_forwards);
 
 /* Test of the device-side timeout path (the pages have no counterpart; it
  * exists so that failure detection can be tested without faulting a GPU).
- * Arms the next moe_forward of `ctx` (FP8-weight format only): every pipeline
- * wait of that forward gives up after `wait_limit_us` microseconds instead of
- * 2 s, and CTA 0's copy producer in GEMM `which` (1 = L1, 2 = L2) never fills
- * its first pipeline stage, so the MMA's wait for it runs out.  That forward
- * returns MOE_OK; its output is undefined; moe_device_status() then returns
- * MOE_ERR_DEVICE_TIMEOUT, and later forwards run normally.  The hook disarms
- * itself after one forward.  Returns MOE_ERR_INVALID_ARG for another `which`
- * or a limit below 1 us, MOE_ERR_UNSUPPORTED for FP4 weights. */
+ * Arms the next moe_forward of `ctx`: every wait of that forward gives up
+ * after `wait_limit_us` microseconds instead of 2 s, and
+ *   which = 1 or 2: CTA 0's copy producer in GEMM `which` (1 = L1, 2 = L2)
+ *           never fills its first pipeline stage, so the MMA's wait for it
+ *           runs out (both weight formats);
+ *   which = 3: CTA 0 of the multi-CTA dispatch (batches of 8192 routed pairs
+ *           or more) never arrives at the grid-wide barrier, so the other
+ *           CTAs' waits run out.
+ * A step of a forward that times out makes that forward's later steps skip
+ * (they check a per-forward abort word at entry) rather than read tables it
+ * left incomplete.  That forward returns MOE_OK; its output is undefined;
+ * moe_device_status() then returns MOE_ERR_DEVICE_TIMEOUT, and later forwards
+ * run normally whether or not the status was read.  The hook disarms itself
+ * after one forward.  Returns MOE_ERR_INVALID_ARG for another `which` or a
+ * limit below 1 us. */
 MOE_API int moe_test_arm_timeout(moe_ctx *ctx, int which, int wait_limit_us);
 
-/* Synchronise the device, read and clear the device error word:
- * MOE_OK, MOE_ERR_BAD_EXPERT, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_CUDA. */
+/* ABI plumbing (the pages define no such call): synchronise the device,
+ * read and clear the device error word: MOE_OK, MOE_ERR_BAD_EXPERT,
+ * MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_CUDA. */
 MOE_API int moe_device_status(moe_ctx *ctx);
 
-/* Static description of an error code. */
+/* ABI plumbing (no counterpart in the pages): static description of an
+ * error code. */
 MOE_API const char *moe_strerror(int code);
 
-/* Free the host state (never the caller's buffers). NULL is allowed. */
+/* ABI plumbing (no counterpart in the pages): free the host state (never
+ * the caller's buffers).  NULL is allowed. */
 MOE_API void moe_destroy(moe_ctx *ctx);
 
 #ifdef __cplusplus

@@ -249,8 +249,9 @@ class MoELayer:
         return int(lib().moe_device_status(self._ctx))
 
     def arm_timeout_test(self, which: int, wait_limit_us: int):
-        """Make the next forward's GEMM `which` (1 = L1, 2 = L2) time out on
-        purpose after `wait_limit_us` (a test of the failure path)."""
+        """Make the next forward time out on purpose after `wait_limit_us`
+        (a test of the failure path): in GEMM `which` (1 = L1, 2 = L2), or at
+        the multi-CTA dispatch's barrier (3, batches of 8192 pairs or more)."""
         _check(lib().moe_test_arm_timeout(self._ctx, int(which), int(wait_limit_us)), "moe_test_arm_timeout")
 
     def close(self):

@@ -68,7 +68,7 @@ Layout make_layout(const moe_config *c) {
         o += bytes;
         return at;
     };
-    L.err = take(sizeof(int) * 4, 256);
+    L.err = take(sizeof(int) * kErrWords, 256);
     L.count = take(4 * E, 256);
     L.offset = take(4 * (E + 1), 256);
     L.mb_prefix = take(4 * (E + 1), 256);
@@ -255,8 +255,10 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     // arrival counters: MOE_FUSED=1 (off by default)
     const char *fz = getenv("MOE_FUSED");
     c->fused = fz && fz[0] == '1';
-    // zero the error word
-    if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * 4) != cudaSuccess) {
+    // zero the error block and the dispatch tables (a first forward that
+    // stops early must not leave later steps uninitialised tables)
+    if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * kErrWords) != cudaSuccess ||
+        cudaMemset(c->ws + c->L.count, 0, c->L.pool - c->L.count) != cudaSuccess) {
         free(c);
         return MOE_ERR_CUDA;
     }
@@ -358,7 +360,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
                                         ctas, s) == cudaSuccess;
         if (!dispatched) (void)cudaGetLastError();
     }
-    if (!dispatched) launch_dispatch(topk_idx, T, k, E, o, s);
+    if (!dispatched && launch_dispatch(topk_idx, T, k, E, o, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (ev) cudaEventRecord(ev[1], s);
 
     // A operand: gather token rows in the L1 producer (tile::gather4) when the
@@ -370,7 +372,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
         tm_x.box[1] = tm_x.box[2] = tm_x.box[0];
     } else {
         launch_pool_gather(static_cast<const uint8_t *>(x), o.gather, o.offset + E, k, H, T * k,
-                           c->w<uint8_t>(L.pool), (int)L.pool_pitch, s);
+                           c->w<uint8_t>(L.pool), (int)L.pool_pitch, o.err, s);
     }
 
     if (g.wfmt == MOE_W_FP4_E2M1_UE8M0_32) {
@@ -399,7 +401,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
         f.b_sf = c->wt_at<uint8_t>(L.w2_sf);
         launch_fp4_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, f, c->num_sms, s);
         if (ev) cudaEventRecord(ev[3], s);
-        launch_combine(f.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);
+        launch_combine(f.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), o.err, s);
         if (ev) cudaEventRecord(ev[4], s);
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
         c->last_T = T;
@@ -467,7 +469,7 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     if (!fused_done) launch_l2(c->tm_l2a, c->tm_w2, c->tm_l2out, p2, c->num_sms, s);
     if (ev) cudaEventRecord(ev[3], s);
 
-    launch_combine(p2.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), s);
+    launch_combine(p2.l2_out, o.pair_pool, T, k, H, static_cast<uint16_t *>(y), o.err, s);
     if (ev) cudaEventRecord(ev[4], s);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     c->last_T = T;
@@ -578,8 +580,8 @@ int moe_profile_end(moe_ctx *c, float *stage_ms, int *n_forwards) {
 }
 
 int moe_test_arm_timeout(moe_ctx *c, int which, int wait_limit_us) {
-    if (!c || (which != kStallL1 && which != kStallL2) || wait_limit_us < 1) return MOE_ERR_INVALID_ARG;
-    if (c->cfg.wfmt != MOE_W_FP8_BLK128) return MOE_ERR_UNSUPPORTED;
+    if (!c || (which != kStallL1 && which != kStallL2 && which != kStallDispatch) || wait_limit_us < 1)
+        return MOE_ERR_INVALID_ARG;
     c->test_hook[0] = wait_limit_us;
     c->test_hook[1] = which;
     c->test_armed = true;

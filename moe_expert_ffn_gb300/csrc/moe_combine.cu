@@ -35,7 +35,8 @@ __device__ __forceinline__ void acc_bf16x2(uint32_t w, float &a, float &b) {
 
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const uint16_t *__restrict__ l2_out, const int32_t *__restrict__ pair_pool, int k,
-                   int H, uint16_t *__restrict__ y) {
+                   int H, uint16_t *__restrict__ y, const int *err) {
+    if (forward_aborted(err)) return;   // an earlier step of this forward timed out
     const int t = blockIdx.x;
     const int h0 = (blockIdx.y * kThreads + threadIdx.x) * kVec;
     if (h0 >= H) return;
@@ -72,9 +73,9 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int k, int H,
-                    uint16_t *y, cudaStream_t s) {
+                    uint16_t *y, const int *err, cudaStream_t s) {
     dim3 grid(T, (H / kVec + kThreads - 1) / kThreads);
-    combine_kernel<<<grid, kThreads, 0, s>>>(l2_out, pair_pool, k, H, y);
+    combine_kernel<<<grid, kThreads, 0, s>>>(l2_out, pair_pool, k, H, y, err);
 }
 
 }  // namespace moe

@@ -16,13 +16,32 @@ constexpr int kErrTimeout = 2;
 // A pipeline wait gives up after this long (a healthy wait lasts microseconds).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
-// The device error block (4 ints in the workspace): [0] error bits, [1] wait
-// limit in microseconds for a test of the timeout path (0 = kWaitTimeoutNs),
-// [2] test stall target (kStallL1 / kStallL2: CTA 0's producer in that GEMM
-// withholds the copies of its first stage), [3] the arrival counter of the
-// multi-CTA dispatch's grid-wide barrier.
+// The device error block (8 ints in the workspace): [0] error bits (sticky
+// until the host reads them), [1] wait limit in microseconds for a test of
+// the timeout path (0 = kWaitTimeoutNs), [2] test stall target (kStallL1 /
+// kStallL2: CTA 0's producer in that GEMM withholds the copies of its first
+// stage; kStallDispatch: CTA 0 of the multi-CTA dispatch withholds its
+// barrier arrival), [3] the arrival counter of the multi-CTA dispatch's
+// grid-wide barrier, [4] this forward's abort word: set with every timeout,
+// cleared when the next forward's dispatch starts, and checked by every
+// later kernel of the forward at entry, so that a forward whose tables were
+// left incomplete skips its remaining steps instead of reading them.
 constexpr int kStallL1 = 1;
 constexpr int kStallL2 = 2;
+constexpr int kStallDispatch = 3;
+constexpr int kErrWords = 8;
+constexpr int kAbortWord = 4;
+
+// A wait ran out: record it for the host and abort the rest of this forward.
+__device__ __forceinline__ void raise_timeout(int *err) {
+    atomicOr(err, kErrTimeout);
+    reinterpret_cast<volatile int *>(err)[kAbortWord] = 1;
+}
+
+// Whether an earlier step of this forward timed out (checked at kernel entry).
+__device__ __forceinline__ bool forward_aborted(const int *err) {
+    return reinterpret_cast<const volatile int *>(err)[kAbortWord] != 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -96,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit) {
             *abort_flag = 1;
-            atomicOr(err, kErrTimeout);
+            raise_timeout(err);
             return false;
         }
     }

@@ -64,7 +64,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kWarps * E; i += kThreads) hist[i] = 0;
-    if (threadIdx.x == 0) bad = 0;
+    if (threadIdx.x == 0) {
+        bad = 0;
+        reinterpret_cast<volatile int *>(o.err)[kAbortWord] = 0;   // a new forward
+    }
     __syncthreads();
 
     const int seg = (P + kWarps - 1) / kWarps;
@@ -147,7 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // separates writing the CTA's per-expert counts from reading every CTA's:
 // each CTA then knows the expert offsets and its own first slot inside each
 // expert, so the stable (token, slot) order holds across CTAs.  CTA 0 writes
-// the per-expert tables.  `bar` is zero before the launch.
+// the per-expert tables.  `bar` and the forward's abort word are zero before
+// the launch; if the barrier runs out, the CTAs return without writing their
+// part and the abort word makes the forward's later kernels skip.
 __global__ void __launch_bounds__(kThreads, 1)
     dispatch_mc_kernel(const int32_t *__restrict__ idx, int T, int k, int E, DispatchOut o,
                        int32_t *__restrict__ cta_cnt, int *bar) {
@@ -194,13 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every CTA's counts written before any is read
     __syncthreads();
     if (threadIdx.x == 0) {
-        red_release_gpu_add(bar, 1);
+        const volatile int *ev = o.err;
+        // timeout-path test: CTA 0 withholds its arrival, so the wait runs out
+        const bool stall = blockIdx.x == 0 && ev[2] == kStallDispatch;
+        if (!stall) red_release_gpu_add(bar, 1);
+        const int lim_us = ev[1];
+        const uint64_t limit = lim_us > 0 ? 1000ull * (uint64_t)lim_us : kWaitTimeoutNs;
         bool ok = true;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_gpu(bar) < (int)gridDim.x) {
             __nanosleep(64);
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                atomicOr(o.err, kErrTimeout);
+            if (globaltimer_ns() - t0 > limit) {
+                raise_timeout(o.err);
                 ok = false;
                 break;
             }
@@ -272,12 +282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256)
     pool_gather_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ gather,
                        const int32_t *__restrict__ offset_E, int k, int H, int rows_bound,
-                       uint8_t *__restrict__ pool, int pool_pitch) {
+                       uint8_t *__restrict__ pool, int pool_pitch, const int *err) {
+    if (forward_aborted(err)) return;   // the dispatch did not finish its tables
     const int P = min(__ldg(offset_E), rows_bound);
     const int lane = threadIdx.x & 31;
     const int vecs = H / 16;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < P; r += (gridDim.x * blockDim.x) >> 5) {
-        const int t = __ldg(gather + r) / k;
+        const int pair = __ldg(gather + r);
+        if ((unsigned)pair >= (unsigned)rows_bound) continue;   // never a pair of this batch
+        const int t = pair / k;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
         uint4 *dst = reinterpret_cast<uint4 *>(pool + (size_t)r * pool_pitch);
         for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
@@ -287,21 +300,28 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *offset_E, int k,
-                        int H, int rows_bound, uint8_t *pool, int pool_pitch, cudaStream_t s) {
+                        int H, int rows_bound, uint8_t *pool, int pool_pitch, const int *err, cudaStream_t s) {
     const int warps = 8;
     const int blocks = max(1, min((rows_bound + warps - 1) / warps, 65535));
     pool_gather_kernel<<<blocks, warps * 32, 0, s>>>(x, gather, offset_E, k, H, rows_bound, pool,
-                                                      pool_pitch);
+                                                      pool_pitch, err);
 }
 
-void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
-                     cudaStream_t s) {
+cudaError_t launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                            cudaStream_t s) {
     const size_t smem = sizeof(int32_t) * (size_t)(kWarps * E + E + 1);
     static std::atomic<uint32_t> smem_set{0};
-    if (smem_limit_once(reinterpret_cast<const void *>(dispatch_kernel), sizeof(int32_t) * (kWarps * 1024 + 1025),
-                        smem_set) != cudaSuccess)
-        return;   // the launch below would fail the same way; the caller's error check reports it
-    dispatch_kernel<<<1, kThreads, smem, s>>>(topk_idx, T, k, E, o);
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void *>(dispatch_kernel),
+                                    sizeof(int32_t) * (kWarps * 1024 + 1025), smem_set);
+    if (e != cudaSuccess) return e;
+    // launched through cudaLaunchKernelEx so that the result is this launch's
+    // own, not an error an earlier, unrelated call left behind
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, dispatch_kernel, topk_idx, T, k, E, o);
 }
 
 cudaError_t launch_dispatch_mc(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
@@ -311,7 +331,8 @@ cudaError_t launch_dispatch_mc(const int32_t *topk_idx, int T, int k, int E, con
     cudaError_t e = smem_limit_once(reinterpret_cast<const void *>(dispatch_mc_kernel),
                                     sizeof(int32_t) * (kWarps * 1024 + 1025), smem_set);
     if (e != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(bar, 0, sizeof(int), s)) != cudaSuccess) return e;
+    // the barrier counter and, next to it, the forward's abort word
+    if ((e = cudaMemsetAsync(bar, 0, 2 * sizeof(int), s)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;   // the grid-wide barrier needs every CTA resident
@@ -346,7 +367,40 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[kNaInts];
 
 constexpr int kNaMaxDevices = 64;
 std::mutex g_noalloc_mu;
-int32_t *g_noalloc_ptr[kNaMaxDevices];
+
+// The array's device address, looked up once per device and context.  The
+// context's ID is kept beside it: after cudaDeviceReset the runtime makes a
+// new primary context (a new ID) in which the library's module, and with it
+// the array, may sit elsewhere, so the address is looked up again.
+struct NoallocSlot {
+    unsigned long long ctx_id;
+    int32_t *ptr;
+};
+NoallocSlot g_noalloc_slot[kNaMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <class Fn>
+Fn driver_fn(const char *name, int version) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// ID of the calling thread's current context, 0 when there is none yet (the
+// runtime binds the primary context on its first call that needs one).
+unsigned long long current_ctx_id() {
+    static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // Device address of g_noalloc_scratch on the current device (host code may
 // not use the symbol itself: on the host it names a stand-in, not the array).
@@ -354,12 +408,15 @@ int noalloc_scratch(int32_t **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocSlot &sl = g_noalloc_slot[dev];
+    const unsigned long long id = current_ctx_id();
+    if (!sl.ptr || id == 0 || id != sl.ctx_id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_noalloc_ptr[dev] = static_cast<int32_t *>(p);
+        sl.ptr = static_cast<int32_t *>(p);
+        sl.ctx_id = current_ctx_id();   // the lookup has bound a context if there was none
     }
-    *out = g_noalloc_ptr[dev];
+    *out = sl.ptr;
     return MOE_OK;
 }
 
@@ -389,6 +446,6 @@ extern "C" MOE_API int moe_dispatch_noalloc(const int32_t *topk_idx, int num_tok
     o.err = scratch + kNaErr;
     // the error word is only ever OR-ed into: start it at zero
     if (cudaMemsetAsync(o.err, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-    moe::launch_dispatch(topk_idx, num_tokens, topk, num_experts, o, s);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return moe::launch_dispatch(topk_idx, num_tokens, topk, num_experts, o, s) == cudaSuccess ? MOE_OK
+                                                                                               : MOE_ERR_CUDA;
 }

@@ -243,7 +243,7 @@ __device__ __forceinline__ bool wait_ready(const int *ready, int mbi, int target
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit) {
             *abort_flag = 1;
-            atomicOr(err, kErrTimeout);
+            raise_timeout(err);
             return false;
         }
     }
@@ -692,6 +692,7 @@ template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kL1Threads, 1)
     l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
               const L1Params p) {
+    if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
@@ -723,6 +724,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
 __global__ void __launch_bounds__(kL2Threads, 1)
     l2_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w2,
               const __grid_constant__ CUtensorMap tm_out, const L2Params p) {
+    if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
@@ -771,6 +773,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
     fused_kernel(const __grid_constant__ AMaps tm_a1, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ AMaps tm_a2, const __grid_constant__ CUtensorMap tm_w2,
                  const __grid_constant__ CUtensorMap tm_out, const L1Params p1, const L2Params p2, int *ready) {
+    if (forward_aborted(p1.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);

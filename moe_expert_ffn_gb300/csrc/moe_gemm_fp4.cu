@@ -106,6 +106,7 @@ template <bool kL1, bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_out, const Fp4Params p) {
+    if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_once = policy_evict_first();
         const uint64_t pol_shared = policy_evict_normal();
         const uint64_t pol_a = policy_evict_last();
+        const bool stall = test_stall(p.err, kL1 ? kStallL1 : kStallL2);
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -176,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (stall && it == 0) continue;   // timeout-path test: never fill the first stage
                 const uint32_t full = smem_u32(&ctrl->full[s]);
                 if (lane == 0) mbar_arrive_expect_tx(full, tx);
                 __syncwarp();

@@ -132,6 +132,7 @@ template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
     l1_pair_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_a3,
                    const __grid_constant__ CUtensorMap tm_w1h, const L1Params p) {
+    if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);

@@ -49,12 +49,13 @@ struct DispatchOut {
     int *err;              // device error word
 };
 
-void launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
-                     cudaStream_t s);
+cudaError_t launch_dispatch(const int32_t *topk_idx, int T, int k, int E, const DispatchOut &o,
+                            cudaStream_t s);
 
 // The same dispatch over `ctas` CTAs of one cooperative launch (large
-// batches): cta_cnt [ctas, E] scratch, bar one int of scratch (zeroed here,
-// in the stream, before the launch).  Fails without launching when not every
+// batches): cta_cnt [ctas, E] scratch; bar = words 3-4 of the error block
+// (the barrier counter and the forward's abort word, both zeroed here, in
+// the stream, before the launch).  Fails without launching when not every
 // CTA can be resident.
 constexpr int kDispatchMcMinPairs = 8192;   // smaller batches: one CTA (measured faster at 4096)
 constexpr int kDispatchMcMaxCtas = 256;
@@ -89,7 +90,7 @@ cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CU
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
 // first offset[E] rows (rows_bound = T*k is the host-side upper bound).
 void launch_pool_gather(const uint8_t *x, const int32_t *gather, const int32_t *offset_E, int k,
-                        int H, int rows_bound, uint8_t *pool, int pool_pitch, cudaStream_t s);
+                        int H, int rows_bound, uint8_t *pool, int pool_pitch, const int *err, cudaStream_t s);
 
 // L2: l2_acts . W2^T with per-64 activation scales, BF16 out in pool order.
 struct L2Params {
@@ -138,7 +139,7 @@ void launch_interleave_rows(const uint8_t *src, uint8_t *dst, int E, int I, int 
 
 // Combine: y[t] = bf16( sum_j bf16 l2_out[pair_pool[t*k+j]] ) in slot order.
 void launch_combine(const uint16_t *l2_out, const int32_t *pair_pool, int T, int k, int H,
-                    uint16_t *y, cudaStream_t s);
+                    uint16_t *y, const int *err, cudaStream_t s);
 
 // Weight transform (W1 gate/up interleave in groups of 8 rows, scale pairs).
 void launch_transform_w1(const uint8_t *w1, const float *w1_sf, uint8_t *w1i, int w1i_pitch,

@@ -60,3 +60,37 @@ def sub_inputs(inp_dev: dict, tokens) -> dict:
     for n in ("w1", "w1_sf", "w2", "w2_sf"):
         out[n] = inp_dev[n][used].cpu().contiguous()
     return out
+
+
+def stratified_tokens(oc, oo, og, k, T, top=3, every_touched=0, seed=0, blocks=True):
+    """Tokens whose pairs reach chosen tiles of a full-size forward.
+
+    From the oracle's dispatch (counts oc, offsets oo, gather og): for each of
+    the `top` largest experts, one pair in every 128-row M block (when
+    `blocks`) and the expert's last pair; with `every_touched` = n, one pair of
+    every n-th touched expert; plus the first and the last token.  Returns the
+    sorted tokens and a description of what they cover."""
+    rng = np.random.default_rng(seed)
+    tok = {0, T - 1}
+    order = np.argsort(-oc, kind="stable")[:top]
+    covered = []
+    for e in order:
+        e = int(e)
+        lo, hi = int(oo[e]), int(oo[e + 1])
+        if hi <= lo:
+            continue
+        nb = (hi - lo + 127) // 128
+        if blocks:
+            for b in range(nb):
+                r = lo + 128 * b + int(rng.integers(0, min(128, hi - lo - 128 * b)))
+                tok.add(int(og[r]) // k)
+        tok.add(int(og[hi - 1]) // k)
+        covered.append(f"expert {e} ({hi - lo} pairs: {'all ' + str(nb) if blocks else 'last of ' + str(nb)} M blocks"
+                       f" + last pair)")
+    if every_touched:
+        touched = np.nonzero(oc > 0)[0]
+        for e in touched[::every_touched]:
+            lo, hi = int(oo[e]), int(oo[e + 1])
+            tok.add(int(og[lo + int(rng.integers(0, hi - lo))]) // k)
+        covered.append(f"one pair of every {every_touched}th of {len(touched)} touched experts")
+    return np.array(sorted(tok), dtype=np.int32), "; ".join(covered)

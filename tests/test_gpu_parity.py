@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import moe_synth
-from gpu_util import assert_y_close, bf16_bits_to_float, compare_y, new_layer, sub_inputs, to_dev
+from gpu_util import assert_y_close, bf16_bits_to_float, compare_y, new_layer, stratified_tokens, sub_inputs, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -343,12 +343,13 @@ def test_full_size_sampled_tokens(m, orc, name):
     counts, offsets, gather = layer.get_dispatch(wl.T)
     st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
     assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
-    rng = np.random.default_rng(7)
-    tokens = np.sort(rng.choice(wl.T, size=6, replace=False)).astype(np.int32)
+    # every M block (and the last pair) of the three largest experts, one pair
+    # of every 16th touched expert, the first and the last token
+    tokens, covered = stratified_tokens(oc, oo, og, wl.k, wl.T, top=3, every_touched=16, seed=7)
     sub = sub_inputs(inp, tokens)
     ref = bf16_bits_to_float(orc.forward(sub))
     rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, name)
-    print(f"{name}: sampled tokens {tokens.tolist()} rel L2 {rel:.2e} max/rms {mx:.2e}")
+    print(f"{name}: {len(tokens)} tokens covering {covered}; rel L2 {rel:.2e} max/rms {mx:.2e}")
     assert torch.isfinite(y.float()).all()
 
 
@@ -360,20 +361,23 @@ def test_largest_batch_sampled_tokens(m, orc):
     inp = moe_synth.make_inputs(wl, device=DEV)
     layer = new_layer(m, wl, DEV)
     layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
+    # the last pair (the last, ragged M block) of the three largest experts,
+    # a few random tokens, the first and the last token
     rng = np.random.default_rng(11)
-    tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=4, replace=False)])).astype(np.int32)
+    tokens, covered = stratified_tokens(oc, oo, og, wl.k, wl.T, top=3, blocks=False, seed=11)
+    tokens = np.unique(np.concatenate([tokens, rng.choice(wl.T, size=4, replace=False)])).astype(np.int32)
     sub = sub_inputs(inp, tokens)   # the oracle needs only the experts these tokens use
     del inp["w1"], inp["w2"]
     y = layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"])
     torch.cuda.synchronize()
     assert layer.device_status() == m.MOE_OK
     counts, offsets, gather = layer.get_dispatch(wl.T)
-    st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
     assert int(oo[-1]) == wl.T * wl.k
     assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
     ref = bf16_bits_to_float(orc.forward(sub))
     rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, "largest")
-    print(f"largest: sampled tokens {tokens.tolist()} rel L2 {rel:.2e} max/rms {mx:.2e}")
+    print(f"largest: tokens {tokens.tolist()} covering {covered}; rel L2 {rel:.2e} max/rms {mx:.2e}")
     assert torch.isfinite(y.float()).all()
 
 
@@ -422,7 +426,9 @@ def test_fp4_full_size_sampled_tokens(m, orc):
     assert layer.device_status() == m.MOE_OK
     counts, _, _ = layer.get_dispatch(wl.T)
     assert (counts.cpu().numpy() == 0).sum() >= wl.n_empty
-    tokens = np.sort(np.random.default_rng(9).choice(wl.T, size=6, replace=False)).astype(np.int32)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"].cpu(), wl.E)
+    assert np.array_equal(counts.cpu().numpy(), oc)
+    tokens, covered = stratified_tokens(oc, oo, og, wl.k, wl.T, top=3, every_touched=16, seed=9)
     ref = bf16_bits_to_float(orc.forward(sub_inputs(inp, tokens), wfmt=1))
     rel, mx = assert_y_close(y[torch.from_numpy(tokens).long().to(DEV)], ref, "fp4")
-    print(f"fp4: rel L2 {rel:.2e} max/rms {mx:.2e}")
+    print(f"fp4: {len(tokens)} tokens covering {covered}; rel L2 {rel:.2e} max/rms {mx:.2e}")
