@@ -179,6 +179,7 @@ struct moe_ctx {
     int last_T;
     CUtensorMap tm_w1, tm_w2;
     CUtensorMap tm_l2out;   // l2_out [Pmax, H] BF16, 32-row x 64-column boxes (L2 epilogue stores)
+    CUtensorMap tm_acts;    // l2_acts [Pmax, I] FP8, 32-row x 64-byte boxes (L1 epilogue stores)
     CUtensorMap tm_w1h;     // FP8 W1i as K panels, 128 rows x 2 panels per box (CTA-pair L1)
     CUtensorMap tm_pool3;   // the pool the same way
     AMaps tm_l2a, tm_pool;
@@ -234,7 +235,9 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
                          make_map_panels(&c->tm_w1h, c->wt + L.w1i, H, E * 2 * I, L.w1_pitch, 128, 2) &&
                          make_map_panels(&c->tm_pool3, c->ws + L.pool, H, Pm, L.pool_pitch, 128, 2) &&
                          make_map(&c->tm_w2, c->wt + L.w2, I, E * H, L.w2_pitch, 128, 256)) &&
-              make_map(&c->tm_l2out, c->ws + L.l2_out, H, Pm, H * 2, 64, 32, CU_TENSOR_MAP_DATA_TYPE_UINT16);
+              make_map(&c->tm_l2out, c->ws + L.l2_out, H, Pm, H * 2, 64, 32, CU_TENSOR_MAP_DATA_TYPE_UINT16) &&
+              make_map(&c->tm_acts, c->ws + L.l2_acts, I, Pm, L.acts_pitch, 64, 32, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
     for (int i = 0; ok && i < 3; ++i)
         ok = make_map(&c->tm_l2a.box[i], c->ws + L.l2_acts, I, Pm, L.acts_pitch, 128, 32u << i) &&
              make_map(&c->tm_pool.box[i], c->ws + L.pool, H, Pm, L.pool_pitch, 128, 32u << i);
@@ -452,17 +455,17 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
         int *ready = c->w<int>(L.ready);
         const size_t ready_bytes = 4 * ((size_t)Pm / kBM + E + 1);
         if (cudaMemsetAsync(ready, 0, ready_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-        fused_done = launch_fused(gather_a ? tm_x : c->tm_pool, c->tm_w1, c->tm_l2a, c->tm_w2, c->tm_l2out, p1, p2,
+        fused_done = launch_fused(gather_a ? tm_x : c->tm_pool, c->tm_w1, c->tm_acts, c->tm_l2a, c->tm_w2, c->tm_l2out, p1, p2,
                                   ready, g.fast_math, gather_a, c->num_sms, s) == cudaSuccess;
         if (!fused_done) (void)cudaGetLastError();
     }
     if (!fused_done) {
         if (pair) {
-            if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_pool3, c->tm_w1h, p1, g.fast_math, gather_a,
+            if (launch_l1_pair(gather_a ? tm_x : c->tm_pool, c->tm_pool3, c->tm_w1h, c->tm_acts, p1, g.fast_math, gather_a,
                                c->num_sms, s) != cudaSuccess)
                 return MOE_ERR_CUDA;
         } else {
-            launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, p1, g.fast_math, gather_a, c->num_sms, s);
+            launch_l1(gather_a ? tm_x : c->tm_pool, c->tm_w1, c->tm_acts, p1, g.fast_math, gather_a, c->num_sms, s);
         }
     }
     if (ev) cudaEventRecord(ev[2], s);

@@ -88,7 +88,11 @@ struct alignas(16) Ctrl {
 
 constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
-constexpr size_t kL1SmemBytes = 1024 + (size_t)kL1Stages * kL1StageBytes + kCtrlBytes;
+// L1 output staging: per epilogue warp 32 rows x 64 FP8 codes (one TMA store
+// box, 64-byte swizzled, 2 KB).
+constexpr uint32_t kL1OutBytes = 32 * 64;
+constexpr size_t kL1SmemBytes =
+    1024 + (size_t)kL1Stages * kL1StageBytes + (size_t)kL1EpiWarps * kL1OutBytes + kCtrlBytes;
 // L2 output staging: per epilogue warp 32 rows x 64 BF16 columns (one TMA
 // store box, 128-byte swizzled), written twice per tile.
 constexpr uint32_t kL2OutBytes = 32 * 128;
@@ -357,8 +361,11 @@ __device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe 
 }
 
 // kSignal: add this warp's finished tiles to the M-block counters in `ready`.
+// out_stage: this warp's 2 KB shared-memory box for the TMA store of its
+// 32 rows x 64 codes (tm_acts: l2_acts with 32-row x 64-byte boxes).
 template <bool kFast, bool kSignal>
-__device__ __forceinline__ void l1_epilogue(const L1Params &p, const Role &r, Pipe &st, int *ready) {
+__device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1Params &p, const Role &r, Pipe &st,
+                                            uint32_t out_stage, int *ready) {
     const int NB = p.I / 128, KB = p.H / kBK;
     const int total = __ldg(p.mb_prefix + p.E) * NB;
     const uint32_t lane = r.lane;
@@ -447,14 +454,42 @@ __device__ __forceinline__ void l1_epilogue(const L1Params &p, const Role &r, Pi
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }
             // this warp's 64 outputs are intermediate columns [64 jb, 64 jb + 64)
-            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + jb * 64);
+            if (q * 32 + 32 <= t.rows) {
+                // all 32 rows of the warp valid: one 32 x 64 box through shared
+                // memory and the copy engine, so each row leaves as one 64-byte
+                // piece instead of 32 rows' 16-byte pieces per instruction
+                // (64-byte swizzle: chunk v of row `lane` at chunk v ^ (lane/2 % 4))
+                if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
+                __syncwarp();
+                const uint32_t rowp = out_stage + lane * 64;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int v = 0; v < 4; ++v)
+                    st_shared_v4(rowp + ((v ^ ((lane >> 1) & 3)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                 pk[4 * v + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tm_acts, jb * 64, t.row0 + q * 32, out_stage);
+                    tma_store_commit();
+                }
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + jb * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
             p.l2_sf[(size_t)row * (p.I / 64) + jb] = sf;
         }
-        if (kSignal) signal_ready(ready, tile / NB, lane);
+        if (kSignal) {
+            // the box's writes complete and ordered before the M block's release
+            if (lane == 0) tma_store_wait_all();
+            __syncwarp();
+            fence_proxy_async_global();
+            signal_ready(ready, tile / NB, lane);
+        }
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- L2 roles
@@ -691,12 +726,13 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kL1Threads, 1)
     l1_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_w1,
-              const L1Params p) {
+              const __grid_constant__ CUtensorMap tm_acts, const L1Params p) {
     if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL1Stages * kL1StageBytes);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL1Stages * kL1StageBytes +
+                                          kL1EpiWarps * kL1OutBytes);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     if (warp == 0 && lane == 0) {
@@ -715,7 +751,8 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         if (!st.ok && st.kt > 0)
             drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL1TBufs]), ((st.kt - 1) / kL1TBufs) & 1, p.err);
     } else {
-        l1_epilogue<kFast, false>(p, r, st, nullptr);
+        l1_epilogue<kFast, false>(tm_acts, p, r, st, base + kL1Stages * kL1StageBytes + (warp - kEpiWarp0) * kL1OutBytes,
+                                  nullptr);
     }
     gemm_teardown(tmem, warp);
 }
@@ -771,8 +808,9 @@ __global__ void __launch_bounds__(kL2Threads, 1)
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kL2Threads, 1)
     fused_kernel(const __grid_constant__ AMaps tm_a1, const __grid_constant__ CUtensorMap tm_w1,
-                 const __grid_constant__ AMaps tm_a2, const __grid_constant__ CUtensorMap tm_w2,
-                 const __grid_constant__ CUtensorMap tm_out, const L1Params p1, const L2Params p2, int *ready) {
+                 const __grid_constant__ CUtensorMap tm_acts, const __grid_constant__ AMaps tm_a2,
+                 const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_out,
+                 const L1Params p1, const L2Params p2, int *ready) {
     if (forward_aborted(p1.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -804,7 +842,9 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         if (!st.ok && st.kt > 0)
             drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL2TBufs]), ((st.kt - 1) / kL2TBufs) & 1, p1.err);
     } else {
-        l1_epilogue<kFast, true>(p1, r, st, ready);
+        // the L1 output box is the first half of the warp's L2 output box
+        l1_epilogue<kFast, true>(tm_acts, p1, r, st,
+                                 base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready);
         if (st.ok)
             l2_epilogue<true, false>(tm_out, p2, r, st,
                               base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready, target);
@@ -816,28 +856,28 @@ __global__ void __launch_bounds__(kL2Threads, 1)
 
 
 template <bool kFast, bool kGatherA>
-static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
+static void launch_l1_t(const AMaps &tm_a, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const L1Params &p,
                         int num_sms, cudaStream_t s) {
     static std::atomic<uint32_t> smem_set{0};
     smem_limit_once(reinterpret_cast<const void *>(l1_kernel<kFast, kGatherA>), kL1SmemBytes, smem_set);
-    l1_kernel<kFast, kGatherA><<<num_sms, kL1Threads, kL1SmemBytes, s>>>(tm_a, tm_w1, p);
+    l1_kernel<kFast, kGatherA><<<num_sms, kL1Threads, kL1SmemBytes, s>>>(tm_a, tm_w1, tm_acts, p);
 }
 
-void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
-               bool gather_a, int num_sms, cudaStream_t s) {
+void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const L1Params &p,
+               int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
     if (fast_math) {
-        if (gather_a) launch_l1_t<true, true>(tm_a, tm_w1, p, num_sms, s);
-        else launch_l1_t<true, false>(tm_a, tm_w1, p, num_sms, s);
+        if (gather_a) launch_l1_t<true, true>(tm_a, tm_w1, tm_acts, p, num_sms, s);
+        else launch_l1_t<true, false>(tm_a, tm_w1, tm_acts, p, num_sms, s);
     } else {
-        if (gather_a) launch_l1_t<false, true>(tm_a, tm_w1, p, num_sms, s);
-        else launch_l1_t<false, false>(tm_a, tm_w1, p, num_sms, s);
+        if (gather_a) launch_l1_t<false, true>(tm_a, tm_w1, tm_acts, p, num_sms, s);
+        else launch_l1_t<false, false>(tm_a, tm_w1, tm_acts, p, num_sms, s);
     }
 }
 
 template <bool kFast, bool kGatherA>
-static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2,
-                                  const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1,
-                                  const L2Params &p2, int *ready, int num_sms, cudaStream_t s) {
+static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts,
+                                  const AMaps &tm_a2, const CUtensorMap &tm_w2, const CUtensorMap &tm_out,
+                                  const L1Params &p1, const L2Params &p2, int *ready, int num_sms, cudaStream_t s) {
     static std::atomic<uint32_t> smem_set{0};
     const cudaError_t e =
         smem_limit_once(reinterpret_cast<const void *>(fused_kernel<kFast, kGatherA>), kL2SmemBytes, smem_set);
@@ -852,17 +892,19 @@ static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_kernel<kFast, kGatherA>, tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<kFast, kGatherA>, tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1,
+                              p2, ready);
 }
 
-cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2, const CUtensorMap &tm_w2,
-                         const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2, int *ready,
-                         int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
+                         const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
+                         int *ready, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
     if (fast_math)
-        return gather_a ? launch_fused_t<true, true>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
-                        : launch_fused_t<true, false>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
-    return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
-                    : launch_fused_t<false, false>(tm_a1, tm_w1, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
+        return gather_a ? launch_fused_t<true, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
+                        : launch_fused_t<true, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms,
+                                                      s);
+    return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
+                    : launch_fused_t<false, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
 }
 
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,

@@ -52,7 +52,10 @@ struct alignas(8) PairCtrl {
 };
 constexpr size_t kCtrlBytes = 512;
 static_assert(sizeof(PairCtrl) <= kCtrlBytes, "ctrl block");
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kCtrlBytes;
+// L1 output staging: per epilogue warp 32 rows x 64 FP8 codes (one TMA store
+// box, 64-byte swizzled, 2 KB).
+constexpr uint32_t kOutBytes = 32 * 64;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kOutBytes + kCtrlBytes;
 
 struct PairTile {
     int e, row0, rows, nb, nmb;   // rows: valid rows of the 256-row block
@@ -131,12 +134,14 @@ __device__ __forceinline__ uint32_t a_copy_bytes(int rows) {
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
     l1_pair_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ CUtensorMap tm_a3,
-                   const __grid_constant__ CUtensorMap tm_w1h, const L1Params p) {
+                   const __grid_constant__ CUtensorMap tm_w1h, const __grid_constant__ CUtensorMap tm_acts,
+                   const L1Params p) {
     if (forward_aborted(p.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = align1024(raw);
-    PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem_raw + (base - raw) + kStages * kStageBytes);
+    PairCtrl *ctrl = reinterpret_cast<PairCtrl *>(smem_raw + (base - raw) + kStages * kStageBytes +
+                                                  kEpiWarps * kOutBytes);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = (warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
         const int lrow = (int)rank * kBM + q * 32 + (int)lane;   // row inside the pair block
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+        const uint32_t out_stage = base + kStages * kStageBytes + (warp - kEpiWarp0) * kOutBytes;
         int kt = 0;
         bool ok = true;
         for (int tile = pair; ok && tile < total; tile += npairs) {
@@ -362,12 +368,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pk[w4] = e4m3x2(qv[0], qv[1]) | (e4m3x2(qv[2], qv[3]) << 16);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + jb * 64);
+            if ((int)rank * kBM + q * 32 + 32 <= t.rows) {
+                // all 32 rows of the warp valid: one 32 x 64 box through
+                // shared memory and the copy engine (64-byte swizzle)
+                if (lane == 0) tma_store_wait_read();   // the previous box has left the buffer
+                __syncwarp();
+                const uint32_t rowp = out_stage + lane * 64;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int v = 0; v < 4; ++v)
+                    st_shared_v4(rowp + ((v ^ ((lane >> 1) & 3)) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                 pk[4 * v + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tm_acts, jb * 64, t.row0 + (int)rank * kBM + q * 32, out_stage);
+                    tma_store_commit();
+                }
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.l2_acts + (size_t)row * p.acts_pitch + jb * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
             p.l2_sf[(size_t)row * (p.I / 64) + jb] = sf;
         }
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
     }
     // Neither CTA leaves (or frees TMEM) while the pair MMA may still touch it.
     tc_fence_before();
@@ -382,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kFast, bool kGatherA>
 static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
-                                 const L1Params &p, int num_sms, cudaStream_t s) {
+                                 const CUtensorMap &tm_acts, const L1Params &p, int num_sms, cudaStream_t s) {
     static std::atomic<int> grids[32];   // per device: the resident-pair grid, 0 until computed
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -412,16 +438,17 @@ static cudaError_t launch_pair_t(const AMaps &tm_a, const CUtensorMap &tm_a3, co
         grids[dev & 31].store(grid, std::memory_order_release);
     }
     cfg.gridDim = dim3(grid);
-    return cudaLaunchKernelEx(&cfg, l1_pair_kernel<kFast, kGatherA>, tm_a, tm_a3, tm_w1h, p);
+    return cudaLaunchKernelEx(&cfg, l1_pair_kernel<kFast, kGatherA>, tm_a, tm_a3, tm_w1h, tm_acts, p);
 }
 
 cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
-                           const L1Params &p, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+                           const CUtensorMap &tm_acts, const L1Params &p, int fast_math, bool gather_a, int num_sms,
+                           cudaStream_t s) {
     if (fast_math)
-        return gather_a ? launch_pair_t<true, true>(tm_a, tm_a3, tm_w1h, p, num_sms, s)
-                        : launch_pair_t<true, false>(tm_a, tm_a3, tm_w1h, p, num_sms, s);
-    return gather_a ? launch_pair_t<false, true>(tm_a, tm_a3, tm_w1h, p, num_sms, s)
-                    : launch_pair_t<false, false>(tm_a, tm_a3, tm_w1h, p, num_sms, s);
+        return gather_a ? launch_pair_t<true, true>(tm_a, tm_a3, tm_w1h, tm_acts, p, num_sms, s)
+                        : launch_pair_t<true, false>(tm_a, tm_a3, tm_w1h, tm_acts, p, num_sms, s);
+    return gather_a ? launch_pair_t<false, true>(tm_a, tm_a3, tm_w1h, tm_acts, p, num_sms, s)
+                    : launch_pair_t<false, false>(tm_a, tm_a3, tm_w1h, tm_acts, p, num_sms, s);
 }
 
 }  // namespace moe

@@ -77,15 +77,18 @@ struct L1Params {
 };
 // gather_a: tm_a maps x [T, H] with one-row boxes (rows gathered in the
 // kernel); otherwise tm_a maps the pool [Pmax, H] with 128-row boxes.
-void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p, int fast_math,
-               bool gather_a, int num_sms, cudaStream_t s);
+// tm_acts: l2_acts [Pmax, I] with 32-row x 64-byte boxes (64-byte swizzle),
+// the TMA stores of the epilogue.
+void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const L1Params &p,
+               int fast_math, bool gather_a, int num_sms, cudaStream_t s);
 
 // L1 on CTA pairs (moe_gemm_pair.cu): 256 x 256 tiles, one M=256 MMA over
 // both CTAs, stages of two 128-K blocks.  tm_a: the 2-D A maps (gather4 from
 // x, or pool boxes); tm_a3 / tm_w1h: the pool / W1i as 3-D [K panel][row][128
 // bytes] with 128-row x 2-panel boxes.  Requires H % 256 == 0.
 cudaError_t launch_l1_pair(const AMaps &tm_a, const CUtensorMap &tm_a3, const CUtensorMap &tm_w1h,
-                           const L1Params &p, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+                           const CUtensorMap &tm_acts, const L1Params &p, int fast_math, bool gather_a, int num_sms,
+                           cudaStream_t s);
 
 // Pool of token rows in dispatch order: pool[r] = x[gather[r] / k] for the
 // first offset[E] rows (rows_bound = T*k is the host-side upper bound).
@@ -104,9 +107,9 @@ struct L2Params {
 // Both FP8 GEMMs in one cooperative launch (L2 tiles wait per M block on
 // the L1 tiles' arrival counters in `ready`, [M blocks] zeroed beforehand).
 // Fails without launching when not every CTA can be resident.
-cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const AMaps &tm_a2, const CUtensorMap &tm_w2,
-                         const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2, int *ready,
-                         int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
+                         const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
+                         int *ready, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
 
 // tm_out: l2_out [Pmax, H] BF16 with 32-row x 64-column boxes (128-byte swizzle).
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
