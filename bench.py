@@ -33,6 +33,13 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL_HBM_GBS = 7900.0     # HBM3e nominal, for context beside the measured copy peak
+# Context figures measured on the GB300s (not the roofline denominators,
+# which come from MEASURED_PEAKS.json): an FP8 E4M3 8192^3 GEMM through
+# torch._scaled_mm (cuBLAS) at a median 1462 MHz under the power cap, and the
+# tcgen05 kind::f8f6f4 issue rate per SM per clock.
+CUBLAS_FP8_TFLOPS = 3371.2
+TCGEN05_FP8_MAC_PER_CLK_SM = 8192
 STAGES = ("dispatch", "l1", "l2", "combine")
 KERNELS = {"dispatch": "dispatch_kernel", "l1": "l1_kernel", "l2": "l2_kernel", "combine": "combine_kernel"}
 
@@ -115,6 +122,24 @@ def roofline_for(stage, wm, seconds, peaks, traffic=None):
         out = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s"}
     out["frac"] = ach / peak
     out["traffic"] = traffic
+    return out
+
+
+def alt_fractions(roof, clk):
+    """The achieved figure against other denominators, for context: HBM-bound
+    kernels against the nominal bandwidth (the measured copy peak counts the
+    bytes of a read+write copy, so a read-mostly stream can pass 1.0 of it),
+    tensor-bound ones against a measured cuBLAS FP8 GEMM and against the
+    tcgen05 FP8 issue rate at the clock sampled during the timed region."""
+    a = roof["achieved"]
+    if roof["bound"] == "hbm":
+        out = {"vs_nominal_hbm": a / NOMINAL_HBM_GBS}
+    else:
+        out = {"vs_cublas_fp8": a / CUBLAS_FP8_TFLOPS}
+        if clk and clk.get("sm_mhz"):
+            rate = TCGEN05_FP8_MAC_PER_CLK_SM * 2 * 152 * clk["sm_mhz"] * 1e6 / 1e12
+            out["vs_tcgen05_rate_at_clock"] = a / rate
+    out["above_measured_peak"] = roof["frac"] > 1.0
     return out
 
 
@@ -375,6 +400,7 @@ def run_ours(args, wl, rank, world, local_rank):
     roof = roofline_for(dom, wm, per_launch[dom] / 1e3, peaks, profiled_traffic(dom, wl.name))
     roof["kernel"] = KERNELS[dom]
     roof["peak_source"] = f"{peaks['source']} ({'HBM copy' if roof['bound'] == 'hbm' else 'bf16 cuBLAS x2 for FP8'})"
+    roof["frac_alt"] = alt_fractions(roof, clk)
     layer_roof = roofline_for("layer", wm, ms / 1e3, peaks)
     tens = peaks["bf16_tflops"] * FP8_OVER_BF16 * 1e12
     t_roof = max(wm["flops"]["layer"] / tens, wm["bytes"]["layer"] / (peaks["hbm_gbs"] * 1e9))
@@ -391,6 +417,7 @@ def run_ours(args, wl, rank, world, local_rank):
                                f"{wm['bytes']['layer'] / 1e9:.2f} GB per step"},
         "tflops": wm["flops"]["layer"] / (ms / 1e3) / 1e12,
         "layer_roofline": {"t_roofline_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3),
+                           "frac_alt": alt_fractions(layer_roof, clk),
                            "bound": layer_roof["bound"], "achieved": layer_roof["achieved"],
                            "unit": layer_roof["unit"]},
         "roofline": roof,

@@ -186,6 +186,7 @@ struct moe_ctx {
     int l1_a_mode;          // 0 auto, 1 gather4 from x, 2 pool
     int l1_pair_mode;       // 0 auto, 1 CTA pairs, 2 single CTAs
     bool fused;             // both FP8 GEMMs in one cooperative launch (MOE_FUSED=1)
+    int split_l1;           // > 0: the two FP8 GEMMs at once on disjoint CTA sets, this many on L1 (MOE_SPLIT)
     int test_hook[2];       // armed timeout test for the next forward: {limit us, stall target}
     bool test_armed;
     cudaEvent_t *prof_ev;   // 5 events per profiled forward
@@ -258,6 +259,19 @@ int moe_create(moe_ctx **out, const moe_config *cfg, void *d_workspace, void *d_
     // arrival counters: MOE_FUSED=1 (off by default)
     const char *fz = getenv("MOE_FUSED");
     c->fused = fz && fz[0] == '1';
+    // the two GEMMs at the same time on disjoint CTA sets of one launch:
+    // MOE_SPLIT=1 (off by default); MOE_SPLIT_L1_SMS sets the L1 share, by
+    // default in proportion to the GEMMs' promotion work (L1: one FP32 pass
+    // per 128-K block over 2I columns, L2: two per 128-K block over H, so
+    // about 2 : 1.4 for equal H and I)
+    const char *sp = getenv("MOE_SPLIT");
+    c->split_l1 = 0;
+    if (sp && sp[0] == '1') {
+        const double w1 = 2.0 * cfg->inter * cfg->hidden, w2 = 1.4 * cfg->hidden * (double)cfg->inter;
+        int n1 = (int)(c->num_sms * w1 / (w1 + w2) + 0.5);
+        if (const char *ns = getenv("MOE_SPLIT_L1_SMS")) n1 = atoi(ns);
+        c->split_l1 = std::max(1, std::min(c->num_sms - 1, n1));
+    }
     // zero the error block and the dispatch tables (a first forward that
     // stops early must not leave later steps uninitialised tables)
     if (cudaMemset(c->ws + c->L.err, 0, sizeof(int) * kErrWords) != cudaSuccess ||
@@ -449,7 +463,17 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     p2.Pmax = Pm;
 
     bool fused_done = false;
-    if (c->fused && !pair) {
+    if (c->split_l1 > 0 && !pair) {
+        // both GEMMs at once on disjoint CTA sets; without room for every CTA
+        // at once it does not launch and the two kernels below run instead
+        int *ready = c->w<int>(L.ready);
+        const size_t ready_bytes = 4 * ((size_t)Pm / kBM + E + 1);
+        if (cudaMemsetAsync(ready, 0, ready_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+        fused_done = launch_split(gather_a ? tm_x : c->tm_pool, c->tm_w1, c->tm_acts, c->tm_l2a, c->tm_w2, c->tm_l2out,
+                                  p1, p2, ready, c->split_l1, g.fast_math, gather_a, c->num_sms, s) == cudaSuccess;
+        if (!fused_done) (void)cudaGetLastError();
+    }
+    if (!fused_done && c->fused && !pair) {
         // one launch for both GEMMs; without room for every CTA at once it
         // does not launch and the two kernels below run instead
         int *ready = c->w<int>(L.ready);

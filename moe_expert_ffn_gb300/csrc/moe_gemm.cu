@@ -81,7 +81,7 @@ struct alignas(16) Ctrl {
     uint64_t tempty[kMaxTBufs];
     uint64_t info_full[kInfoSlots];
     uint64_t info_empty[kInfoSlots];
-    int4 info[kInfoSlots];   // e, row0, rows, nb
+    int4 info[kInfoSlots];   // e, row0, rows | nb << 8, global M block
     uint32_t tmem_base;
     int abort;
 };
@@ -142,7 +142,7 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem, int warp) {
 __device__ __forceinline__ bool put_tile(Ctrl *ctrl, int tc, const Tile &t, volatile int *abort_flag, int *err) {
     const int i = tc % kInfoSlots;
     if (!mbar_wait(smem_u32(&ctrl->info_empty[i]), ((tc / kInfoSlots) & 1) ^ 1, abort_flag, err)) return false;
-    ctrl->info[i] = make_int4(t.e, t.row0, t.rows, t.nb);
+    ctrl->info[i] = make_int4(t.e, t.row0, t.rows | (t.nb << 8), t.mbi);
     mbar_arrive(smem_u32(&ctrl->info_full[i]));   // release: the slot's contents come first
     return true;
 }
@@ -155,8 +155,9 @@ __device__ __forceinline__ bool get_tile(Ctrl *ctrl, int tc, Tile &t, uint32_t l
     const volatile int *v = reinterpret_cast<const volatile int *>(&ctrl->info[i]);
     t.e = v[0];
     t.row0 = v[1];
-    t.rows = v[2];
-    t.nb = v[3];
+    t.rows = v[2] & 0xff;
+    t.nb = v[2] >> 8;
+    t.mbi = v[3];
     t.nmb = 0;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&ctrl->info_empty[i]));
@@ -223,12 +224,15 @@ struct Role {
     volatile int *abort_flag;
     uint32_t lane;
     int warp;
+    int cta, ncta;   // this CTA's tiles of the GEMM: cta, cta + ncta, ...
 };
 
 // M-block readiness between the GEMMs of one launch: every L1 epilogue warp
-// adds one to its tile's M-block counter after its stores; an L2 tile waits
-// until the counter holds all of that block's L1 tiles (column blocks x
-// epilogue warps).  Bounded like the barrier waits.
+// adds one to its tile's M-block counter (the tile's global M block, not its
+// place in the tile list, which N-major experts walk column block first)
+// after its stores; an L2 tile waits until the counter of its M block holds
+// all of that block's L1 tiles (column blocks x epilogue warps).  Bounded
+// like the barrier waits.
 __device__ __forceinline__ void signal_ready(int *ready, int mbi, uint32_t lane) {
     fence_acq_rel_gpu();   // this lane's stores before the warp's release
     __syncwarp();
@@ -269,20 +273,20 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_shared = policy_evict_normal();
     const uint64_t pol_x = policy_evict_last();
-    const bool stall = test_stall(p.err, kStallL1);
+    const bool stall = test_stall(p.err, kStallL1, r.cta);
     const int it0 = st.it;   // this GEMM's first stage
     // the next tile is decoded during this one (its dependent loads would
     // otherwise hold back the copies at every tile start)
     const int kb_fin = min(1, KB - 1);
     TilePrefetch pf;
-    if ((int)blockIdx.x < total) {
-        pf.begin(blockIdx.x, NB, p.mblk_expert);
+    if (r.cta < total) {
+        pf.begin(r.cta, NB, p.mblk_expert);
         pf.finish(p.offset, p.mb_prefix);
     }
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         const Tile t = pf.tile(NB);
-        const bool has_next = tile + (int)gridDim.x < total;
-        if (has_next) pf.begin(tile + gridDim.x, NB, p.mblk_expert);
+        const bool has_next = tile + r.ncta < total;
+        if (has_next) pf.begin(tile + r.ncta, NB, p.mblk_expert);
         bool put_ok = true;
         if (lane == 0) put_ok = put_tile(ctrl, st.tc, t, r.abort_flag, p.err);
         if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
@@ -334,7 +338,7 @@ __device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe 
     const int total = __ldg(p.mb_prefix + p.E) * NB;
     Ctrl *ctrl = r.ctrl;
     constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta) {
         for (int kb = 0; kb < KB; ++kb, ++st.it, ++st.kt) {
             const int s = st.it % kL1Stages;
             const uint32_t ph = (st.it / kL1Stages) & 1;
@@ -374,7 +378,7 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
     const int h = (r.warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
     const int lrow = q * 32 + (int)lane;
     const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         Tile t;
         if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
             st.ok = false;
@@ -485,7 +489,7 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
             if (lane == 0) tma_store_wait_all();
             __syncwarp();
             fence_proxy_async_global();
-            signal_ready(ready, tile / NB, lane);
+            signal_ready(ready, t.mbi, lane);
         }
     }
     if (lane == 0) tma_store_wait_all();
@@ -504,26 +508,26 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_shared = policy_evict_normal();
     const uint64_t pol_a = policy_evict_last();
-    const bool stall = test_stall(p.err, kStallL2);
+    const bool stall = test_stall(p.err, kStallL2, r.cta);
     const int it0 = st.it;   // this GEMM's first stage
     int last_mbi = -1;
     // the next tile is decoded during this one, as in the L1 producer
     const int kb_fin = min(1, KB - 1);
     TilePrefetch pf;
-    if ((int)blockIdx.x < total) {
-        pf.begin(blockIdx.x, NB, p.mblk_expert);
+    if (r.cta < total) {
+        pf.begin(r.cta, NB, p.mblk_expert);
         pf.finish(p.offset, p.mb_prefix);
     }
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         const Tile t = pf.tile(NB);
-        const bool has_next = tile + (int)gridDim.x < total;
-        if (has_next) pf.begin(tile + gridDim.x, NB, p.mblk_expert);
+        const bool has_next = tile + r.ncta < total;
+        if (has_next) pf.begin(tile + r.ncta, NB, p.mblk_expert);
         if (!put_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
             st.ok = false;
             break;
         }
-        if (ready && tile / NB != last_mbi) {
-            last_mbi = tile / NB;
+        if (ready && t.mbi != last_mbi) {
+            last_mbi = t.mbi;
             if (!wait_ready(ready, last_mbi, target, r.abort_flag, p.err)) {
                 st.ok = false;
                 break;
@@ -563,7 +567,7 @@ __device__ __forceinline__ void l2_issue(const L2Params &p, const Role &r, Pipe 
     const int total = __ldg(p.mb_prefix + p.E) * NB;
     Ctrl *ctrl = r.ctrl;
     constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL2BN);
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta) {
         for (int kb = 0; st.ok && kb < KB; ++kb, ++st.it) {
             const int s = st.it % kL2Stages;
             const uint32_t ph = (st.it / kL2Stages) & 1;
@@ -616,7 +620,7 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
     const int lrow = q * 32 + (int)lane;
     const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
     const int HB = p.H / 128;                  // 128-row weight scale blocks
-    for (int tile = blockIdx.x; st.ok && tile < total; tile += gridDim.x, ++st.tc) {
+    for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         Tile t;
         if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
             st.ok = false;
@@ -624,7 +628,7 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
         }
         if (kAcquire) {
             bool rd = true;
-            if (lane == 0) rd = wait_ready(ready, tile / NB, target, r.abort_flag, p.err);
+            if (lane == 0) rd = wait_ready(ready, t.mbi, target, r.abort_flag, p.err);
             if (!__shfl_sync(0xffffffffu, rd, 0)) {
                 st.ok = false;
                 break;
@@ -741,7 +745,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         tma_prefetch_desc(&tm_w1);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL1Stages, kL1TBufs, kL1EpiWarps);
-    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp, (int)blockIdx.x, (int)gridDim.x};
     Pipe st;
     if (warp == 0) {
         l1_produce<kGatherA>(tm_a, tm_w1, p, r, st);
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         tma_prefetch_desc(&tm_w2);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
-    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp, (int)blockIdx.x, (int)gridDim.x};
     Pipe st;
     if (warp == 0) {
         if (lane == 0) {
@@ -826,7 +830,7 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         tma_prefetch_desc(&tm_w2);
     }
     const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
-    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp};
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp, (int)blockIdx.x, (int)gridDim.x};
     const int target = (p1.I / 128) * kL1EpiWarps;   // L1 tile-warps per M block
     Pipe st;
     if (warp == 0) {
@@ -848,6 +852,79 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         if (st.ok)
             l2_epilogue<true, false>(tm_out, p2, r, st,
                               base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready, target);
+    }
+    gemm_teardown(tmem, warp);
+}
+
+// The overlapped split of the two GEMMs on disjoint SM sets (PR357
+// Green-Context Split MegaMoE code review, §5.2 "SM 资源划分" and §6.2 "K2"):
+// L1 and L2 run at the same time, each on its own CTAs, and an L2 tile starts
+// on an M block as soon as that block's L1 tiles have stored their outputs.
+// On one GPU this is one cooperative launch (every CTA resident) whose CTAs
+// are partitioned: CTAs [0, n1) walk the L1 tiles, CTAs [n1, grid) the L2
+// tiles, through the per-M-block arrival counters of fused_kernel.  Two
+// separate launches spinning on each other's counters would rely on both being
+// resident at once, which nothing guarantees; one cooperative launch does.
+template <bool kFast, bool kGatherA>
+__global__ void __launch_bounds__(kL2Threads, 1)
+    split_kernel(const __grid_constant__ AMaps tm_a1, const __grid_constant__ CUtensorMap tm_w1,
+                 const __grid_constant__ CUtensorMap tm_acts, const __grid_constant__ AMaps tm_a2,
+                 const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_out,
+                 const L1Params p1, const L2Params p2, int *ready, int n1) {
+    if (forward_aborted(p1.err)) return;   // an earlier step of this forward timed out
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align1024(raw);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL2Stages * kL2StageBytes +
+                                          kL2EpiWarps * kL2OutBytes);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const bool is_l1 = (int)blockIdx.x < n1;
+    if (warp == 0 && lane == 0) {
+        if (is_l1) {
+            tma_prefetch_desc(&tm_a1.box[0]);
+            tma_prefetch_desc(&tm_w1);
+        } else {
+            tma_prefetch_desc(&tm_a2.box[2]);
+            tma_prefetch_desc(&tm_w2);
+        }
+    }
+    const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
+    const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp, is_l1 ? (int)blockIdx.x : (int)blockIdx.x - n1,
+                 is_l1 ? n1 : (int)gridDim.x - n1};
+    const uint32_t out_stage = base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes;
+    const int target = (p1.I / 128) * kL1EpiWarps;   // L1 tile-warps per M block
+    Pipe st;
+    if (is_l1) {
+        if (warp == 0) {
+            l1_produce<kGatherA>(tm_a1, tm_w1, p1, r, st);
+            if (!st.ok) drain_producer(ctrl, st.it, kL1Stages, p1.err);
+        } else if (warp == 1) {
+            l1_issue(p1, r, st);
+            if (!st.ok && st.kt > 0)
+                drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL1TBufs]), ((st.kt - 1) / kL1TBufs) & 1, p1.err);
+        } else {
+            l1_epilogue<kFast, true>(tm_acts, p1, r, st, out_stage, ready);
+        }
+    } else {
+        if (warp == 0) {
+            if (lane == 0) {
+                l2_produce(tm_a2, tm_w2, p2, r, st, ready, target);
+                if (!st.ok) drain_producer(ctrl, st.it, kL2Stages, p2.err);
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            l2_issue<true>(p2, r, st);
+            if (!st.ok && st.kt > 0) {   // the last committed use: a first half (tfull) or a stage (empty)
+                const int u = st.kt - 1;
+                if (u & 1)
+                    drain_wait(smem_u32(&ctrl->empty[(u >> 1) % kL2Stages]), ((u >> 1) / kL2Stages) & 1, p2.err);
+                else
+                    drain_wait(smem_u32(&ctrl->tfull[u % kL2TBufs]), (u / kL2TBufs) & 1, p2.err);
+            }
+        } else {
+            l2_epilogue<true, true>(tm_out, p2, r, st, out_stage, ready, target);
+        }
     }
     gemm_teardown(tmem, warp);
 }
@@ -905,6 +982,44 @@ cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUt
                                                       s);
     return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
                     : launch_fused_t<false, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
+}
+
+template <bool kFast, bool kGatherA>
+static cudaError_t launch_split_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts,
+                                  const AMaps &tm_a2, const CUtensorMap &tm_w2, const CUtensorMap &tm_out,
+                                  const L1Params &p1, const L2Params &p2, int *ready, int n1, int num_sms,
+                                  cudaStream_t s) {
+    static std::atomic<uint32_t> smem_set{0};
+    const cudaError_t e =
+        smem_limit_once(reinterpret_cast<const void *>(split_kernel<kFast, kGatherA>), kL2SmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: L2 CTAs wait on the L1 CTAs' counters
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kL2Threads);
+    cfg.dynamicSmemBytes = kL2SmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kernel<kFast, kGatherA>, tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1,
+                              p2, ready, n1);
+}
+
+cudaError_t launch_split(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
+                         const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
+                         int *ready, int n1, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+    if (n1 < 1 || n1 >= num_sms) return cudaErrorInvalidValue;
+    if (fast_math)
+        return gather_a ? launch_split_t<true, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, n1,
+                                                     num_sms, s)
+                        : launch_split_t<true, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, n1,
+                                                      num_sms, s);
+    return gather_a ? launch_split_t<false, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, n1,
+                                                  num_sms, s)
+                    : launch_split_t<false, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, n1,
+                                                   num_sms, s);
 }
 
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,

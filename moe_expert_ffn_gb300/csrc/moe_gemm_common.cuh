@@ -9,6 +9,7 @@ namespace moe {
 
 struct Tile {
     int e, row0, rows, nb, nmb;   // nmb: M blocks of expert e
+    int mbi;                      // global index of the tile's M block (mb_prefix[e] + its block in e)
 };
 
 // Tile `tile` of a grouped GEMM with NB column blocks: experts in ascending
@@ -31,6 +32,7 @@ __device__ __forceinline__ Tile make_tile(int tile, int NB, int e, int first, in
     t.rows = min(kBM, cnt - mb * kBM);
     t.nb = nb;
     t.nmb = nmb;
+    t.mbi = first + mb;
     return t;
 }
 
@@ -80,10 +82,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
         if (globaltimer_ns() - t0 > limit) return;
 }
 
-// Test of the timeout path: whether CTA 0's producer in GEMM `which` withholds
+// Test of the timeout path: whether the producer of the first CTA of GEMM
+// `which` (cta: the CTA's index among the CTAs that run that GEMM) withholds
 // the copies of its first stage (so the MMA's wait for them runs out).
-__device__ __forceinline__ bool test_stall(const int *err, int which) {
-    return blockIdx.x == 0 && reinterpret_cast<const volatile int *>(err)[2] == which;
+__device__ __forceinline__ bool test_stall(const int *err, int which, int cta) {
+    return cta == 0 && reinterpret_cast<const volatile int *>(err)[2] == which;
 }
 
 

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_once = policy_evict_first();
         const uint64_t pol_shared = policy_evict_normal();
         const uint64_t pol_a = policy_evict_last();
-        const bool stall = test_stall(p.err, kL1 ? kStallL1 : kStallL2);
+        const bool stall = test_stall(p.err, kL1 ? kStallL1 : kStallL2, blockIdx.x);
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {

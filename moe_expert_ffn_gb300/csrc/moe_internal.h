@@ -111,6 +111,14 @@ cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUt
                          const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
                          int *ready, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
 
+// The two FP8 GEMMs at the same time on disjoint CTA sets of one cooperative
+// launch: CTAs [0, n1) run L1, the other num_sms - n1 run L2, each L2 tile
+// waiting on its M block's counter in `ready` ([M blocks], zeroed
+// beforehand).  Fails without launching when not every CTA can be resident.
+cudaError_t launch_split(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
+                         const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
+                         int *ready, int n1, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+
 // tm_out: l2_out [Pmax, H] BF16 with 32-row x 64-column boxes (128-byte swizzle).
 void launch_l2(const AMaps &tm_a, const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L2Params &p,
                int num_sms, cudaStream_t s);

@@ -32,12 +32,15 @@ def m():
     return mod
 
 
-@pytest.mark.parametrize("fused", ["0", "1"], ids=["two_launches", "one_launch"])
+@pytest.mark.parametrize("mode", ["two", "fused", "split"], ids=["two_launches", "one_launch", "split_launch"])
 @pytest.mark.parametrize("which", [1, 2], ids=["l1", "l2"])
-def test_timeout_is_reported_and_context_recovers(m, which, fused, monkeypatch):
+def test_timeout_is_reported_and_context_recovers(m, which, mode, monkeypatch):
     # one_launch: both GEMMs in one kernel, where L2 tiles of other CTAs also
-    # wait (bounded) for the M block the withheld stage belongs to
-    monkeypatch.setenv("MOE_FUSED", fused)
+    # wait (bounded) for the M block the withheld stage belongs to; split: the
+    # first CTA of the L1 (or of the L2) CTA set withholds its stage, and the
+    # L2 CTAs waiting on that M block give up too
+    monkeypatch.setenv("MOE_FUSED", "1" if mode == "fused" else "0")
+    monkeypatch.setenv("MOE_SPLIT", "1" if mode == "split" else "0")
     wl = moe_synth.custom(T=96, H=512, I=256, E=4, k=2, seed=71)
     inp = to_dev(moe_synth.make_inputs(wl), DEV)
     layer = new_layer(m, wl, DEV)

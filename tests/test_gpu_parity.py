@@ -181,6 +181,46 @@ def test_fused_launch_full_size(m, name, monkeypatch):
     assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
 
 
+# Both FP8 GEMMs at the same time on disjoint CTA sets of one cooperative
+# launch (MOE_SPLIT=1): L2 tiles start on an M block as soon as its L1 tiles
+# are stored, so y must again be bit-identical to the two launches.  The L1
+# share is the default and, to make L2 CTAs wait on many M blocks, 8 CTAs.
+@pytest.mark.parametrize("l1_sms", ["", "8"], ids=["default_share", "l1_8_ctas"])
+@pytest.mark.parametrize("wl", FUSED_CASES, ids=lambda w: w.name)
+def test_split_launch_matches_two_launches(m, orc, wl, l1_sms, monkeypatch):
+    inp = moe_synth.make_inputs(wl)
+    if wl.name == "fused_counts":
+        inp["topk_idx"] = _crafted_counts(wl.T, wl.k, wl.E, [1, 127, 128, 129, 255, 256, 257, 47], wl.seed)
+    monkeypatch.setenv("MOE_SPLIT", "0")
+    _, _, y2 = _run(m, wl, inp)
+    monkeypatch.setenv("MOE_SPLIT", "1")
+    if l1_sms:
+        monkeypatch.setenv("MOE_SPLIT_L1_SMS", l1_sms)
+    _, _, y1 = _run(m, wl, inp)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref = bf16_bits_to_float(orc.forward(inp))
+    rel, mx = assert_y_close(y1, ref, f"{wl.name}/split")
+    print(f"{wl.name}/split{l1_sms}: bit-identical to two launches, rel L2 {rel:.2e}")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_split_launch_full_size(m, name, monkeypatch):
+    """Full sizes in the bench's launch configuration: the split launch's y
+    equals the two-launch y bit for bit."""
+    wl = moe_synth.WORKLOADS[name]
+    inp = moe_synth.make_inputs(wl, device=DEV)
+    ys = []
+    for split in ("0", "1"):
+        monkeypatch.setenv("MOE_SPLIT", split)
+        layer = new_layer(m, wl, DEV)
+        layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+        ys.append(layer.forward(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"]).clone())
+        torch.cuda.synchronize()
+        assert layer.device_status() == m.MOE_OK
+        del layer
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+
+
 @pytest.mark.parametrize("clamp", [float("inf"), 1.0], ids=["noclamp", "clamp1"])
 @pytest.mark.parametrize("fast", [0, 1], ids=["expf", "fastexp"])
 @pytest.mark.parametrize("variant", ["single", "pairs", "fp4"])
