@@ -37,6 +37,7 @@
 #include "moe_device.cuh"
 #include "moe_gemm_common.cuh"
 #include "moe_internal.h"
+#include "moe_phases.cuh"
 
 namespace moe {
 namespace {
@@ -265,7 +266,7 @@ template <bool kGatherA>
 __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap &tm_w1, const L1Params &p,
                                            const Role &r, Pipe &st) {
     const int NB = p.I / 128, KB = p.H / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     const uint32_t lane = r.lane;
     Ctrl *ctrl = r.ctrl;
     // weights of an expert with one M block are read once (evict first);
@@ -299,7 +300,7 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int rr = (int)lane * 4 + i;
-                tok[i] = rr < t.rows ? __ldg(p.gather + t.row0 + rr) / p.k : 0;
+                tok[i] = rr < t.rows ? __ldcg(p.gather + t.row0 + rr) / p.k : 0;
             }
         }
         const int wrow = t.e * 2 * p.I + t.nb * kL1BN;
@@ -335,7 +336,7 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
 
 __device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe &st) {
     const int NB = p.I / 128, KB = p.H / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     Ctrl *ctrl = r.ctrl;
     constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL1BN);
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta) {
@@ -371,7 +372,7 @@ template <bool kFast, bool kSignal>
 __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1Params &p, const Role &r, Pipe &st,
                                             uint32_t out_stage, int *ready) {
     const int NB = p.I / 128, KB = p.H / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     const uint32_t lane = r.lane;
     Ctrl *ctrl = r.ctrl;
     const int q = r.warp & 3;                  // TMEM lane quadrant this warp may access
@@ -387,7 +388,7 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
         const bool valid = lrow < t.rows;
         const bool warp_on = q * 32 < t.rows;
         const int row = t.row0 + lrow;
-        const int pair = valid ? __ldg(p.gather + row) : 0;
+        const int pair = valid ? __ldcg(p.gather + row) : 0;
         // the pair's top-k weight, needed only by the tail: load it now
         const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
         const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
@@ -503,7 +504,7 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
                                            const Role &r, Pipe &st, const int *ready, int target) {
     const int NB = (p.H + kL2BN - 1) / kL2BN;   // the last block may be half empty (H % 256 == 128)
     const int KB = p.I / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     Ctrl *ctrl = r.ctrl;
     const uint64_t pol_once = policy_evict_first();
     const uint64_t pol_shared = policy_evict_normal();
@@ -564,7 +565,7 @@ template <bool kOneCommit>
 __device__ __forceinline__ void l2_issue(const L2Params &p, const Role &r, Pipe &st) {
     const int NB = (p.H + kL2BN - 1) / kL2BN;
     const int KB = p.I / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     Ctrl *ctrl = r.ctrl;
     constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kL2BN);
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta) {
@@ -612,7 +613,7 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
                                             uint32_t out_stage, const int *ready, int target) {
     const int NB = (p.H + kL2BN - 1) / kL2BN;
     const int KB = p.I / kBK;
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
     const uint32_t lane = r.lane;
     Ctrl *ctrl = r.ctrl;
     const int q = r.warp & 3;
@@ -803,18 +804,23 @@ __global__ void __launch_bounds__(kL2Threads, 1)
     gemm_teardown(tmem, warp);
 }
 
-// Both GEMMs in one persistent launch (every CTA resident: a cooperative
-// launch).  Each CTA runs its L1 tiles and then its L2 tiles through the same
-// stage ring, accumulators and tile ring; an L2 tile starts once the L1 tiles
-// of its M block (on any CTA) have stored their outputs, so L2 work fills the
-// SMs that finish L1 early (the pages' fused pipeline with arrival counters,
-// design §3.3, on one GPU).
+// The whole forward in one persistent launch (every CTA resident: a
+// cooperative launch), the pages' fused pipeline (MegaMoE SM90 Implementation
+// Design (Final), §3.3): Phase 1 the dispatch over all CTAs with grid-wide
+// barriers, then the pool copy of the token rows; Phases 2 and 3 each CTA's
+// L1 tiles and then its L2 tiles through the same stage ring, accumulators
+// and tile ring, an L2 tile starting once the L1 tiles of its M block (on
+// any CTA) have stored their outputs, so L2 work fills the SMs that finish
+// L1 early; Phase 4, after a last barrier, the combine.  On one GPU the
+// pages' NVLink pull, scatter and barriers are the local pool copy, the
+// pool-order outputs and these grid barriers.  The dispatch's scratch lives
+// in the stage ring, which the pipeline only uses after it.
 template <bool kFast, bool kGatherA>
 __global__ void __launch_bounds__(kL2Threads, 1)
     fused_kernel(const __grid_constant__ AMaps tm_a1, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_acts, const __grid_constant__ AMaps tm_a2,
                  const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_out,
-                 const L1Params p1, const L2Params p2, int *ready) {
+                 const L1Params p1, const L2Params p2, int *ready, const FusedParams f) {
     if (forward_aborted(p1.err)) return;   // an earlier step of this forward timed out
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -829,6 +835,24 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         tma_prefetch_desc(&tm_a2.box[2]);
         tma_prefetch_desc(&tm_w2);
     }
+    // ---- Phase 1: dispatch, then the pool of token rows
+    int bar_target = 0;
+    {
+        const bool stall = blockIdx.x == 0 && reinterpret_cast<const volatile int *>(p1.err)[2] == kStallDispatch;
+        bool ok = dispatch_phase(f.topk_idx, f.T, f.k, p1.E, f.d, f.cta_cnt, f.bar, bar_target,
+                                 reinterpret_cast<int32_t *>(smem_raw + (base - raw)), stall);
+        if (ok && !kGatherA) {
+            pool_phase(f.x, f.d.gather, f.d.offset + p1.E, f.k, p1.H, f.T * f.k, f.pool, f.pool_pitch);
+            bar_target += (int)gridDim.x;
+            ok = grid_sync(f.bar, bar_target, p1.err);
+        }
+        if (!ok) return;   // a barrier ran out; no TMEM held yet
+        // the generic writes of the dispatch scratch (shared) and of the pool
+        // (global) before the copy engine touches either
+        fence_async_smem();
+        fence_proxy_async_global();
+    }
+    // ---- Phases 2 and 3: the two GEMMs
     const uint32_t tmem = gemm_setup(ctrl, warp, kL2Stages, kL2TBufs, kL2EpiWarps);
     const Role r{ctrl, base, tmem, &ctrl->abort, lane, warp, (int)blockIdx.x, (int)gridDim.x};
     const int target = (p1.I / 128) * kL1EpiWarps;   // L1 tile-warps per M block
@@ -852,8 +876,15 @@ __global__ void __launch_bounds__(kL2Threads, 1)
         if (st.ok)
             l2_epilogue<true, false>(tm_out, p2, r, st,
                               base + kL2Stages * kL2StageBytes + (warp - kEpiWarp0) * kL2OutBytes, ready, target);
+        // this warp's output stores are complete (the epilogue waited for
+        // them); order them before the barrier's release, for the combine
+        fence_proxy_async_global();
     }
     gemm_teardown(tmem, warp);
+    // ---- Phase 4: the combine, once every CTA's L2 outputs are stored
+    bar_target += (int)gridDim.x;
+    if (!grid_sync(f.bar, bar_target, p1.err) || forward_aborted(p1.err)) return;
+    combine_phase(p2.l2_out, f.d.pair_pool, f.T, f.k, p2.H, f.y);
 }
 
 // The overlapped split of the two GEMMs on disjoint SM sets (PR357
@@ -954,7 +985,8 @@ void launch_l1(const AMaps &tm_a, const CUtensorMap &tm_w1, const CUtensorMap &t
 template <bool kFast, bool kGatherA>
 static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts,
                                   const AMaps &tm_a2, const CUtensorMap &tm_w2, const CUtensorMap &tm_out,
-                                  const L1Params &p1, const L2Params &p2, int *ready, int num_sms, cudaStream_t s) {
+                                  const L1Params &p1, const L2Params &p2, int *ready, const FusedParams &f,
+                                  int num_sms, cudaStream_t s) {
     static std::atomic<uint32_t> smem_set{0};
     const cudaError_t e =
         smem_limit_once(reinterpret_cast<const void *>(fused_kernel<kFast, kGatherA>), kL2SmemBytes, smem_set);
@@ -970,18 +1002,22 @@ static cudaError_t launch_fused_t(const AMaps &tm_a1, const CUtensorMap &tm_w1, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fused_kernel<kFast, kGatherA>, tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1,
-                              p2, ready);
+                              p2, ready, f);
 }
 
 cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
                          const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
-                         int *ready, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+                         int *ready, const FusedParams &f, int fast_math, bool gather_a, int num_sms, cudaStream_t s) {
+    if (num_sms > kDispatchMcMaxCtas || p1.E > 1024) return cudaErrorInvalidValue;
     if (fast_math)
-        return gather_a ? launch_fused_t<true, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
-                        : launch_fused_t<true, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms,
-                                                      s);
-    return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s)
-                    : launch_fused_t<false, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, num_sms, s);
+        return gather_a ? launch_fused_t<true, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, f,
+                                                     num_sms, s)
+                        : launch_fused_t<true, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, f,
+                                                      num_sms, s);
+    return gather_a ? launch_fused_t<false, true>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, f,
+                                                  num_sms, s)
+                    : launch_fused_t<false, false>(tm_a1, tm_w1, tm_acts, tm_a2, tm_w2, tm_out, p1, p2, ready, f,
+                                                   num_sms, s);
 }
 
 template <bool kFast, bool kGatherA>

@@ -52,15 +52,17 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__r
 // or so later) the expert's offsets; tile() then needs no load.
 struct TilePrefetch {
     int tl, e, first, first1, off, off1;
+    // L2-coherent loads: the one-launch forward writes these tables earlier
+    // in the same launch
     __device__ __forceinline__ void begin(int tile, int NB, const int32_t *mblk_expert) {
         tl = tile;
-        e = __ldg(mblk_expert + tile / NB);
+        e = __ldcg(mblk_expert + tile / NB);
     }
     __device__ __forceinline__ void finish(const int32_t *offset, const int32_t *mb_prefix) {
-        first = __ldg(mb_prefix + e);
-        first1 = __ldg(mb_prefix + e + 1);
-        off = __ldg(offset + e);
-        off1 = __ldg(offset + e + 1);
+        first = __ldcg(mb_prefix + e);
+        first1 = __ldcg(mb_prefix + e + 1);
+        off = __ldcg(offset + e);
+        off1 = __ldcg(offset + e + 1);
     }
     __device__ __forceinline__ Tile tile(int NB) const {
         return make_tile(tl, NB, e, first, first1 - first, off, off1 - off);

@@ -104,12 +104,26 @@ struct L2Params {
     int *err;
     int H, I, E, Pmax;
 };
-// Both FP8 GEMMs in one cooperative launch (L2 tiles wait per M block on
-// the L1 tiles' arrival counters in `ready`, [M blocks] zeroed beforehand).
-// Fails without launching when not every CTA can be resident.
+// What the one-launch forward needs besides the GEMMs' parameters.
+struct FusedParams {
+    const int32_t *topk_idx;   // [T, k]
+    int T, k;
+    DispatchOut d;             // the dispatch tables it writes (mb2 tables unused)
+    int32_t *cta_cnt;          // [grid, E] scratch
+    int *bar;                  // grid-barrier counter; zero, with the abort word after it, before the launch
+    const uint8_t *x;          // token rows, copied into `pool` unless L1 gathers them itself
+    uint8_t *pool;
+    int pool_pitch;
+    uint16_t *y;               // [T, H]
+};
+// The whole FP8 forward in one cooperative launch: dispatch, pool copy, both
+// GEMMs (L2 tiles wait per M block on the L1 tiles' arrival counters in
+// `ready`, [M blocks] zeroed beforehand) and the combine, with grid-wide
+// barriers between the phases.  Fails without launching when not every CTA
+// can be resident (or num_sms > kDispatchMcMaxCtas, E > 1024).
 cudaError_t launch_fused(const AMaps &tm_a1, const CUtensorMap &tm_w1, const CUtensorMap &tm_acts, const AMaps &tm_a2,
                          const CUtensorMap &tm_w2, const CUtensorMap &tm_out, const L1Params &p1, const L2Params &p2,
-                         int *ready, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
+                         int *ready, const FusedParams &f, int fast_math, bool gather_a, int num_sms, cudaStream_t s);
 
 // The two FP8 GEMMs at the same time on disjoint CTA sets of one cooperative
 // launch: CTAs [0, n1) run L1, the other num_sms - n1 run L2, each L2 tile

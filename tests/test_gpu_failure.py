@@ -71,9 +71,12 @@ def test_arm_rejects_bad_arguments(m):
             layer.arm_timeout_test(which, lim)
 
 
-def test_dispatch_barrier_timeout_is_reported_and_skips_the_forward(m):
+@pytest.mark.parametrize("fused", ["0", "1"], ids=["dispatch_kernel", "one_launch"])
+def test_dispatch_barrier_timeout_is_reported_and_skips_the_forward(m, fused, monkeypatch):
     # 8192 routed pairs: the dispatch runs over 8 CTAs with a grid-wide
-    # barrier; the hook makes CTA 0 withhold its arrival
+    # barrier (or, in the one-launch forward, over every CTA); the hook makes
+    # CTA 0 withhold its arrival
+    monkeypatch.setenv("MOE_FUSED", fused)
     wl = moe_synth.custom(T=2048, H=256, I=128, E=64, k=4, seed=72, routing="zipf")
     inp = to_dev(moe_synth.make_inputs(wl), DEV)
     layer = new_layer(m, wl, DEV)

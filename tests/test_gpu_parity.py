@@ -141,10 +141,11 @@ def test_l1_cta_pairs_match_oracle(m, orc, wl, a_mode, monkeypatch):
     print(f"{wl.name}/pairs/{a_mode}: rel L2 {rel:.2e}, max/rms {mx:.2e}")
 
 
-# Both FP8 GEMMs in one cooperative launch (MOE_FUSED=1): the same
-# arithmetic as the two launches, so y must be bit-identical to theirs; and
-# within tolerance of the oracle.  Small cases plus an expert mix where many
-# M blocks finish their L1 tiles at different times.
+# The whole FP8 forward in one cooperative launch (MOE_FUSED=1: dispatch,
+# pool copy, both GEMMs, combine, with grid barriers between the phases): the
+# same arithmetic as the separate kernels, so y must be bit-identical to
+# theirs, and the dispatch maps equal to the oracle's.  Small cases plus an
+# expert mix where many M blocks finish their L1 tiles at different times.
 FUSED_CASES = SMALL + [moe_synth.custom(T=600, H=512, I=256, E=8, k=2, seed=38, name="fused_counts")]
 
 
@@ -156,11 +157,41 @@ def test_fused_launch_matches_two_launches(m, orc, wl, monkeypatch):
     monkeypatch.setenv("MOE_FUSED", "0")
     _, _, y2 = _run(m, wl, inp)
     monkeypatch.setenv("MOE_FUSED", "1")
-    _, _, y1 = _run(m, wl, inp)
+    layer, _, y1 = _run(m, wl, inp)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    counts, offsets, gather = layer.get_dispatch(wl.T)
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"], wl.E)
+    assert np.array_equal(counts.cpu().numpy(), oc) and np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(gather.cpu().numpy()[: oo[-1]], og)
     ref = bf16_bits_to_float(orc.forward(inp))
     rel, mx = assert_y_close(y1, ref, f"{wl.name}/fused")
-    print(f"{wl.name}/fused: bit-identical to two launches, rel L2 {rel:.2e}")
+    print(f"{wl.name}/fused: bit-identical to the separate kernels, rel L2 {rel:.2e}")
+
+
+def test_fused_launch_inactive_slots_bad_ids_and_stats(m, orc, monkeypatch):
+    """The one-launch dispatch skips inactive slots, reports an out-of-range
+    expert id (and skips it), and adds the counts to the caller's statistics."""
+    monkeypatch.setenv("MOE_FUSED", "1")
+    wl = moe_synth.custom(T=300, H=256, I=128, E=16, k=3, seed=39, name="fused_slots")
+    inp = moe_synth.make_inputs(wl)
+    inp["topk_idx"][::3, 1] = -1
+    inp["topk_idx"][7, :] = -1
+    layer = new_layer(m, wl, DEV)
+    g = to_dev(inp, DEV)
+    layer.transform_weights(g["w1"], g["w1_sf"], g["w2"], g["w2_sf"])
+    stats = torch.zeros(wl.E, dtype=torch.int32, device=DEV)
+    y = layer.forward(g["x"], g["x_sf"], g["topk_idx"], g["topk_weights"], stats=stats)
+    y = layer.forward(g["x"], g["x_sf"], g["topk_idx"], g["topk_weights"], stats=stats)
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    st, oc, oo, og = orc.dispatch(inp["topk_idx"], wl.E)
+    assert np.array_equal(stats.cpu().numpy(), 2 * oc)
+    assert torch.all(y[7] == 0)
+    assert_y_close(y, bf16_bits_to_float(orc.forward(inp)), "fused inactive slots")
+    bad = g["topk_idx"].clone()
+    bad[11, 2] = wl.E + 5
+    layer.forward(g["x"], g["x_sf"], bad, g["topk_weights"])
+    assert layer.device_status() == m.MOE_ERR_BAD_EXPERT
 
 
 @pytest.mark.parametrize("name", ["decode", "prefill"])
