@@ -42,6 +42,15 @@ CUBLAS_FP8_TFLOPS = 3371.2
 TCGEN05_FP8_MAC_PER_CLK_SM = 8192
 STAGES = ("dispatch", "l1", "l2", "combine")
 KERNELS = {"dispatch": "dispatch_kernel", "l1": "l1_kernel", "l2": "l2_kernel", "combine": "combine_kernel"}
+KERNELS_FP4 = dict(KERNELS, l1="fp4_gemm_kernel_l1", l2="fp4_gemm_kernel_l2")
+
+
+def kernel_name(stage, wl):
+    """The library kernel that runs a stage of this workload (the dispatch
+    over several CTAs for batches of 8192 routed pairs or more)."""
+    if stage == "dispatch" and wl.T * wl.k >= 8192:
+        return "dispatch_mc_kernel"
+    return (KERNELS_FP4 if wl.wfmt == 1 else KERNELS)[stage]
 
 
 def parse_args():
@@ -152,10 +161,10 @@ def launches_per_forward(wl):
     return 4 if gather else 5
 
 
-def profiled_traffic(stage, workload):
+def profiled_traffic(stage, wl):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload (a line `traffic_bytes_per_launch: N`), or None."""
-    path = os.path.join(ROOT, "profiles", f"{KERNELS[stage]}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel_name(stage, wl)}_{wl.name}.md")
     try:
         with open(path) as fh:
             for line in fh:
@@ -397,8 +406,8 @@ def run_ours(args, wl, rank, world, local_rank):
     wm = work_model(wl, counts)
     per_launch = {s: stage_ms[s] / max(nfw, 1) for s in STAGES}
     dom = max(("l1", "l2", "combine", "dispatch"), key=lambda s: per_launch[s])
-    roof = roofline_for(dom, wm, per_launch[dom] / 1e3, peaks, profiled_traffic(dom, wl.name))
-    roof["kernel"] = KERNELS[dom]
+    roof = roofline_for(dom, wm, per_launch[dom] / 1e3, peaks, profiled_traffic(dom, wl))
+    roof["kernel"] = kernel_name(dom, wl)
     roof["peak_source"] = f"{peaks['source']} ({'HBM copy' if roof['bound'] == 'hbm' else 'bf16 cuBLAS x2 for FP8'})"
     roof["frac_alt"] = alt_fractions(roof, clk)
     layer_roof = roofline_for("layer", wm, ms / 1e3, peaks)
