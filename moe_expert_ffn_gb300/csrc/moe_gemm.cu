@@ -25,15 +25,21 @@
 //              columns per warp): tcgen05.ld each finished accumulator,
 //              release it, and FMA it into FP32 registers with its scale
 //              product (the pages' "promotion"); after the last block,
-//              SwiGLU/requantise (L1) or BF16 (L2) and store.  The L2 output
-//              goes through a per-warp shared-memory box and a TMA store, so
-//              each row leaves as whole 128-byte pieces instead of 32 rows'
-//              16-byte pieces per instruction.
+//              SwiGLU/requantise (L1) or BF16 (L2) and store.  Both outputs
+//              go through per-warp shared-memory boxes and TMA stores, so
+//              each row leaves as whole 64- or 128-byte pieces instead of 32
+//              rows' 16-byte pieces per instruction.
 // L1: 128 x 256 tiles (128 gate/up pairs = two 64-column output groups), two
 // 256-column accumulators, one per 128-K block.  L2: 128 x 256 tiles, two
 // 256-column accumulators, one per 64-K half.  Register budget: 168 per
 // thread; each epilogue thread keeps 128 accumulators and loads TMEM in
-// 16-column pieces so nothing spills.
+// 16-column pieces.
+//
+// Besides one kernel per GEMM, the same warp roles make two single-launch
+// variants: fused_kernel, the whole forward (dispatch, pool copy, both GEMMs,
+// combine) in one cooperative launch, and split_kernel, both GEMMs at the
+// same time on disjoint CTA sets; in both, L2 tiles wait on per-M-block
+// arrival counters that the L1 epilogues release.
 #include "moe_device.cuh"
 #include "moe_gemm_common.cuh"
 #include "moe_internal.h"
