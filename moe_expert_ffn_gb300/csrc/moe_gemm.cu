@@ -9,8 +9,9 @@
 // rounded to BF16.
 //
 // Both kernels are persistent (one CTA per SM) and walk a tile list derived
-// on the device from the dispatch counts (design §12: experts in order,
-// N-major inside experts with many rows).  Warp roles, 10 warps:
+// on the device from the dispatch counts (design §12: N-major inside experts
+// with many rows; the tiles of one-block experts, whose weights are read once
+// from HBM, spread evenly among the others).  Warp roles, 10 warps:
 //   warp 0     TMA producer: multi-stage smem ring (A: 128 rows x 128 K bytes,
 //              token rows gathered from x with tile::gather4 or one 2-D box of
 //              the pool; B: weight rows x 128 K bytes);
@@ -28,7 +29,13 @@
 //              SwiGLU/requantise (L1) or BF16 (L2) and store.  Both outputs
 //              go through per-warp shared-memory boxes and TMA stores, so
 //              each row leaves as whole 64- or 128-byte pieces instead of 32
-//              rows' 16-byte pieces per instruction.
+//              rows' 16-byte pieces per instruction.  A tile's fields stay in
+//              its tile-ring slot until the tail, so the K loop holds only
+//              the accumulators, the loaded piece and the scale state;
+//   warp 10    (stand-alone L1 kernel) tile loader: for each published tile
+//              the rows' dependent loads (pool row -> pair -> top-k weight,
+//              token scale row -> first scale) into a shared-memory table, so
+//              an epilogue warp starts a tile without global-load latency.
 // L1: 128 x 256 tiles (128 gate/up pairs = two 64-column output groups), two
 // 256-column accumulators, one per 128-K block.  L2: 128 x 256 tiles, two
 // 256-column accumulators, one per 64-K half.  Register budget: 168 per
@@ -50,7 +57,8 @@ namespace {
 
 constexpr int kEpiWarp0 = 2;                 // warps 2.. run the epilogue
 constexpr int kL1EpiWarps = 8;               // L1: two warps per TMEM lane quadrant
-constexpr int kL1Threads = 32 * (kEpiWarp0 + kL1EpiWarps);
+constexpr int kL1Threads = 32 * (kEpiWarp0 + kL1EpiWarps + 1);   // + the tile loader (last warp)
+constexpr int kL1LoaderWarp = kEpiWarp0 + kL1EpiWarps;
 constexpr int kL2EpiWarps = 8;               // L2: two warps per TMEM lane quadrant
 constexpr int kL2Threads = 32 * (kEpiWarp0 + kL2EpiWarps);
 constexpr uint32_t kTmemCols = 512;
@@ -91,15 +99,28 @@ struct alignas(16) Ctrl {
     int4 info[kInfoSlots];   // e, row0, rows | nb << 8, global M block
     uint32_t tmem_base;
     int abort;
+    float stash[kL2EpiWarps][32];   // per epilogue warp: a per-row value the tile's tail needs (L1: top-k weight)
+    uint64_t rows_full[kInfoSlots];  // L1 tile loader: the slot's per-row table is written
 };
 
-constexpr size_t kCtrlBytes = 512;
+// What the L1 tile loader writes per tile-ring slot: for each of the tile's
+// 128 rows its top-k weight, the offset of its token's scale row and that
+// row's first scale, and the tile's two first weight-scale pairs.
+struct alignas(16) L1Rows {
+    float wgt[kBM];
+    int sfa[kBM];
+    float sa0[kBM];
+    float2 sb0[2];
+};
+constexpr size_t kL1RowsBytes = kInfoSlots * sizeof(L1Rows);
+
+constexpr size_t kCtrlBytes = 1536;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "ctrl block");
 // L1 output staging: per epilogue warp 32 rows x 64 FP8 codes (one TMA store
 // box, 64-byte swizzled, 2 KB).
 constexpr uint32_t kL1OutBytes = 32 * 64;
 constexpr size_t kL1SmemBytes =
-    1024 + (size_t)kL1Stages * kL1StageBytes + (size_t)kL1EpiWarps * kL1OutBytes + kCtrlBytes;
+    1024 + (size_t)kL1Stages * kL1StageBytes + (size_t)kL1EpiWarps * kL1OutBytes + kCtrlBytes + kL1RowsBytes;
 // L2 output staging: per epilogue warp 32 rows x 64 BF16 columns (one TMA
 // store box, 128-byte swizzled), written twice per tile.
 constexpr uint32_t kL2OutBytes = 32 * 128;
@@ -120,6 +141,7 @@ __device__ __forceinline__ uint32_t gemm_setup(Ctrl *ctrl, int warp, int stages,
             mbar_init(smem_u32(&ctrl->tempty[b]), epi_warps);
         }
         for (int i = 0; i < kInfoSlots; ++i) {
+            mbar_init(smem_u32(&ctrl->rows_full[i]), 1);
             mbar_init(smem_u32(&ctrl->info_full[i]), 1);
             mbar_init(smem_u32(&ctrl->info_empty[i]), epi_warps);
         }
@@ -154,21 +176,30 @@ __device__ __forceinline__ bool put_tile(Ctrl *ctrl, int tc, const Tile &t, vola
     return true;
 }
 
-// Epilogue side: read tile number tc and free its slot (every epilogue warp).
-__device__ __forceinline__ bool get_tile(Ctrl *ctrl, int tc, Tile &t, uint32_t lane, volatile int *abort_flag,
-                                         int *err) {
-    const int i = tc % kInfoSlots;
-    if (!mbar_wait(smem_u32(&ctrl->info_full[i]), (tc / kInfoSlots) & 1, abort_flag, err)) return false;
-    const volatile int *v = reinterpret_cast<const volatile int *>(&ctrl->info[i]);
+__device__ __forceinline__ Tile tile_at(Ctrl *ctrl, int tc) {
+    const volatile int *v = reinterpret_cast<const volatile int *>(&ctrl->info[tc % kInfoSlots]);
+    Tile t;
     t.e = v[0];
     t.row0 = v[1];
     t.rows = v[2] & 0xff;
     t.nb = v[2] >> 8;
     t.mbi = v[3];
     t.nmb = 0;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&ctrl->info_empty[i]));
+    return t;
+}
+
+// Epilogue side, in two steps: wait for tile number tc and read it, keeping
+// its slot; the tail reads it again (tile_at) and frees it (free_tile), so
+// the tile's fields need no registers during the tile.
+__device__ __forceinline__ bool peek_tile(Ctrl *ctrl, int tc, Tile &t, volatile int *abort_flag, int *err) {
+    const int i = tc % kInfoSlots;
+    if (!mbar_wait(smem_u32(&ctrl->info_full[i]), (tc / kInfoSlots) & 1, abort_flag, err)) return false;
+    t = tile_at(ctrl, tc);
     return true;
+}
+__device__ __forceinline__ void free_tile(Ctrl *ctrl, int tc, uint32_t lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctrl->info_empty[tc % kInfoSlots]));
 }
 
 // Release TMEM buffer b to the MMA warp (one arrival per epilogue warp).
@@ -285,15 +316,17 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
     // the next tile is decoded during this one (its dependent loads would
     // otherwise hold back the copies at every tile start)
     const int kb_fin = min(1, KB - 1);
+    int n_tiles, singles;
+    tile_counts(p.mb_prefix, p.E, NB, n_tiles, singles);
     TilePrefetch pf;
     if (r.cta < total) {
-        pf.begin(r.cta, NB, p.mblk_expert);
+        pf.begin(tile_at_position(r.cta, n_tiles, singles), NB, p.mblk_expert);
         pf.finish(p.offset, p.mb_prefix);
     }
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         const Tile t = pf.tile(NB);
         const bool has_next = tile + r.ncta < total;
-        if (has_next) pf.begin(tile + r.ncta, NB, p.mblk_expert);
+        if (has_next) pf.begin(tile_at_position(tile + r.ncta, n_tiles, singles), NB, p.mblk_expert);
         bool put_ok = true;
         if (lane == 0) put_ok = put_tile(ctrl, st.tc, t, r.abort_flag, p.err);
         if (!__shfl_sync(0xffffffffu, put_ok, 0)) {
@@ -340,6 +373,43 @@ __device__ __forceinline__ void l1_produce(const AMaps &tm_a, const CUtensorMap 
     }
 }
 
+// The L1 tile loader (one warp): for each tile the producer publishes, the
+// rows' dependent loads (pool row -> pair -> top-k weight and token scale
+// row -> first scale) and the first weight scales, into the slot's L1Rows
+// table, so that an epilogue warp starts a tile with shared-memory reads
+// instead of three dependent global loads.  It reads the slot after the
+// producer publishes it and never frees it (the epilogue does, after the
+// tail), so a table is rewritten only after its tile's epilogue is done.
+__device__ __forceinline__ void l1_load_rows(const L1Params &p, const Role &r, L1Rows *rows) {
+    const int NB = p.I / 128, KB = p.H / kBK;
+    const int total = __ldcg(p.mb_prefix + p.E) * NB;
+    Ctrl *ctrl = r.ctrl;
+    int tc = 0;
+    for (int tile = r.cta; tile < total; tile += r.ncta, ++tc) {
+        const int i = tc % kInfoSlots;
+        if (!mbar_wait(smem_u32(&ctrl->info_full[i]), (tc / kInfoSlots) & 1, r.abort_flag, p.err)) return;
+        const Tile t = tile_at(ctrl, tc);
+        L1Rows &R = rows[i];
+        int pr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int rr = (int)r.lane + 32 * j;
+            pr[j] = rr < t.rows ? __ldcg(p.gather + t.row0 + rr) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int rr = (int)r.lane + 32 * j;
+            const int off = (pr[j] / p.k) * KB;
+            R.wgt[rr] = rr < t.rows ? __ldg(p.topk_w + pr[j]) : 0.0f;
+            R.sfa[rr] = off;
+            R.sa0[rr] = __ldg(p.x_sf + off);
+        }
+        if (r.lane < 2) R.sb0[r.lane] = __ldg(p.w1_sf + (t.e * (2 * NB) + t.nb * 2 + (int)r.lane) * KB);
+        __syncwarp();
+        if (r.lane == 0) mbar_arrive(smem_u32(&ctrl->rows_full[i]));
+    }
+}
+
 __device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe &st) {
     const int NB = p.I / 128, KB = p.H / kBK;
     const int total = __ldcg(p.mb_prefix + p.E) * NB;
@@ -374,9 +444,9 @@ __device__ __forceinline__ void l1_issue(const L1Params &p, const Role &r, Pipe 
 // kSignal: add this warp's finished tiles to the M-block counters in `ready`.
 // out_stage: this warp's 2 KB shared-memory box for the TMA store of its
 // 32 rows x 64 codes (tm_acts: l2_acts with 32-row x 64-byte boxes).
-template <bool kFast, bool kSignal>
+template <bool kFast, bool kSignal, bool kRows = false>
 __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1Params &p, const Role &r, Pipe &st,
-                                            uint32_t out_stage, int *ready) {
+                                            uint32_t out_stage, int *ready, const L1Rows *rows = nullptr) {
     const int NB = p.I / 128, KB = p.H / kBK;
     const int total = __ldcg(p.mb_prefix + p.E) * NB;
     const uint32_t lane = r.lane;
@@ -385,37 +455,58 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
     const int h = (r.warp - kEpiWarp0) >> 2;   // which 128 of the 256 tile columns
     const int lrow = q * 32 + (int)lane;
     const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+    float *wstash = ctrl->stash[r.warp - kEpiWarp0];
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
-        Tile t;
-        if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
-            st.ok = false;
-            break;
+        // Tile state for the K loop only: offsets of the two scale rows and
+        // whether the warp holds any row.  What the tail needs is read again
+        // from the tile ring (its slot is held until then) and, for the top-k
+        // weight, from shared memory, so none of it occupies registers
+        // during the promotion.
+        bool warp_on;
+        int sfa_off, sfb_off;
+        float sa_n;
+        float2 sb_n;
+        {
+            Tile t;
+            if (!peek_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
+                st.ok = false;
+                break;
+            }
+            warp_on = q * 32 < t.rows;
+            sfb_off = (t.e * (2 * NB) + t.nb * 2 + h) * KB;   // interleaved 128-row block = output 64-group
+            if (kRows) {
+                const int i = st.tc % kInfoSlots;
+                if (!mbar_wait(smem_u32(&ctrl->rows_full[i]), (st.tc / kInfoSlots) & 1, r.abort_flag, p.err)) {
+                    st.ok = false;
+                    break;
+                }
+                sfa_off = rows[i].sfa[lrow];
+                sa_n = rows[i].sa0[lrow];
+                sb_n = rows[i].sb0[h];
+            } else {
+                const bool valid = lrow < t.rows;
+                const int pair = valid ? __ldcg(p.gather + t.row0 + lrow) : 0;
+                wstash[lane] = valid ? __ldg(p.topk_w + pair) : 0.0f;
+                sfa_off = (pair / p.k) * KB;
+                // (an invalid row reads token 0's scales: in bounds, and its
+                // outputs are not stored)
+                sa_n = __ldg(p.x_sf + sfa_off);
+                sb_n = __ldg(p.w1_sf + sfb_off);
+            }
         }
-        const bool valid = lrow < t.rows;
-        const bool warp_on = q * 32 < t.rows;
-        const int row = t.row0 + lrow;
-        const int pair = valid ? __ldcg(p.gather + row) : 0;
-        // the pair's top-k weight, needed only by the tail: load it now
-        const float wgt = valid ? __ldg(p.topk_w + pair) : 0.0f;
-        const int jb = t.nb * 2 + h;     // interleaved 128-row block = output 64-group
-        const float2 *sfb = p.w1_sf + ((size_t)t.e * (2 * NB) + jb) * KB;
-        const float *sfa = p.x_sf + (size_t)(pair / p.k) * KB;
 
         float2 acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
         // scale factors prefetched one K block ahead
-        float sa_n = valid ? __ldg(sfa) : 0.0f;
-        float2 sb_n = __ldg(sfb);
         for (int kb = 0; kb < KB; ++kb, ++st.kt) {
             const int b = st.kt % kL1TBufs;
             const uint32_t tph = (st.kt / kL1TBufs) & 1;
-            const float sa = sa_n;
-            const float2 sb = sb_n;
+            const float s_lo = sa_n * sb_n.x, s_hi = sa_n * sb_n.y;
             if (kb + 1 < KB) {
-                sa_n = valid ? __ldg(sfa + kb + 1) : 0.0f;
-                sb_n = __ldg(sfb + kb + 1);
+                sa_n = __ldg(p.x_sf + sfa_off + kb + 1);
+                sb_n = __ldg(p.w1_sf + sfb_off + kb + 1);
             }
             if (!mbar_wait(smem_u32(&ctrl->tfull[b]), tph, r.abort_flag, p.err)) {
                 st.ok = false;
@@ -423,11 +514,15 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
             }
             tc_fence_after();
             if (warp_on)
-                promote128(acc, t_lane + b * kL1BN, sa * sb.x, sa * sb.y, ctrl, b, lane);
+                promote128(acc, t_lane + b * kL1BN, s_lo, s_hi, ctrl, b, lane);
             else
                 release_tbuf(ctrl, b, lane);
         }
         if (!st.ok) break;
+        const Tile t = tile_at(ctrl, st.tc);
+        const int row = t.row0 + lrow;
+        const int jb = t.nb * 2 + h;
+        const bool valid = lrow < t.rows;
         if (valid) {
             // SwiGLU * top-k weight (gate columns 0-7, up columns 8-15 of every 16)
             const float clampv = p.clamp;
@@ -443,7 +538,7 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
                     silu = __fdividef(g, 1.0f + __expf(-g));
                 else
                     silu = __fdividef(g, 1.0f + expf(-g));
-                const float a = silu * u * wgt;
+                const float a = silu * u * (kRows ? rows[st.tc % kInfoSlots].wgt[lrow] : wstash[lane]);
                 act[o] = a;
                 amax = fmaxf(amax, fabsf(a));
             }
@@ -491,6 +586,7 @@ __device__ __forceinline__ void l1_epilogue(const CUtensorMap &tm_acts, const L1
             }
             p.l2_sf[(size_t)row * (p.I / 64) + jb] = sf;
         }
+        free_tile(ctrl, st.tc, lane);
         if (kSignal) {
             // the box's writes complete and ordered before the M block's release
             if (lane == 0) tma_store_wait_all();
@@ -520,15 +616,17 @@ __device__ __forceinline__ void l2_produce(const AMaps &tm_a, const CUtensorMap 
     int last_mbi = -1;
     // the next tile is decoded during this one, as in the L1 producer
     const int kb_fin = min(1, KB - 1);
+    int n_tiles, singles;
+    tile_counts(p.mb_prefix, p.E, NB, n_tiles, singles);
     TilePrefetch pf;
     if (r.cta < total) {
-        pf.begin(r.cta, NB, p.mblk_expert);
+        pf.begin(tile_at_position(r.cta, n_tiles, singles), NB, p.mblk_expert);
         pf.finish(p.offset, p.mb_prefix);
     }
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
         const Tile t = pf.tile(NB);
         const bool has_next = tile + r.ncta < total;
-        if (has_next) pf.begin(tile + r.ncta, NB, p.mblk_expert);
+        if (has_next) pf.begin(tile_at_position(tile + r.ncta, n_tiles, singles), NB, p.mblk_expert);
         if (!put_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
             st.ok = false;
             break;
@@ -628,27 +726,34 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
     const uint32_t t_lane = r.tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
     const int HB = p.H / 128;                  // 128-row weight scale blocks
     for (int tile = r.cta; st.ok && tile < total; tile += r.ncta, ++st.tc) {
-        Tile t;
-        if (!get_tile(ctrl, st.tc, t, lane, r.abort_flag, p.err)) {
-            st.ok = false;
-            break;
-        }
-        if (kAcquire) {
-            bool rd = true;
-            if (lane == 0) rd = wait_ready(ready, t.mbi, target, r.abort_flag, p.err);
-            if (!__shfl_sync(0xffffffffu, rd, 0)) {
+        // K-loop state only (the tail reads the tile again from its slot)
+        bool warp_on;
+        int sfa_off, sfb_off;
+        {
+            Tile t;
+            if (!peek_tile(ctrl, st.tc, t, r.abort_flag, p.err)) {
                 st.ok = false;
                 break;
             }
-            __syncwarp();   // lane 0's acquire before every lane's loads
+            if (kAcquire) {
+                bool rd = true;
+                if (lane == 0) rd = wait_ready(ready, t.mbi, target, r.abort_flag, p.err);
+                if (!__shfl_sync(0xffffffffu, rd, 0)) {
+                    st.ok = false;
+                    break;
+                }
+                __syncwarp();   // lane 0's acquire before every lane's loads
+            }
+            const int cb = t.nb * 2 + h;           // this warp's 128-column block of H
+            warp_on = q * 32 < t.rows && cb < HB;
+            sfb_off = (t.e * HB + min(cb, HB - 1)) * KB;
+            // the row's two 64-K activation scales of 128-K block kb (a row
+            // past the tile's end reads the tile's last row: in bounds, and
+            // its outputs are not stored)
+            sfa_off = (t.row0 + min(lrow, t.rows - 1)) * (p.I / 128);
         }
-        const int cb = t.nb * 2 + h;           // this warp's 128-column block of H
-        const bool cols_ok = cb < HB;
-        const bool valid = lrow < t.rows && cols_ok;
-        const bool warp_on = q * 32 < t.rows && cols_ok;
-        const float *sfb = p.w2_sf + ((size_t)t.e * HB + min(cb, HB - 1)) * KB;
-        // the row's two 64-K activation scales of 128-K block kb: sfa[kb]
-        const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf + (size_t)(t.row0 + lrow) * (p.I / 64));
+        const float2 *sfa = reinterpret_cast<const float2 *>(p.l2_sf) + sfa_off;
+        const float *sfb = p.w2_sf + sfb_off;
 
         float2 acc[64];
 #pragma unroll
@@ -657,8 +762,8 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
         // scales prefetched two 128-K blocks ahead (a far L2 hit takes
         // longer than one block's promotion)
         const float2 z2 = make_float2(0.0f, 0.0f);
-        float2 sa0 = valid ? load_sa<kAcquire>(sfa) : z2;
-        float2 sa1 = (valid && KB > 1) ? load_sa<kAcquire>(sfa + 1) : z2;
+        float2 sa0 = load_sa<kAcquire>(sfa);
+        float2 sa1 = KB > 1 ? load_sa<kAcquire>(sfa + 1) : z2;
         float sb0 = __ldg(sfb);
         float sb1 = KB > 1 ? __ldg(sfb + 1) : 0.0f;
         for (int kb = 0; st.ok && kb < KB; ++kb) {
@@ -667,7 +772,7 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
             sa0 = sa1;
             sb0 = sb1;
             if (kb + 2 < KB) {
-                if (valid) sa1 = load_sa<kAcquire>(sfa + kb + 2);
+                sa1 = load_sa<kAcquire>(sfa + kb + 2);
                 sb1 = __ldg(sfb + kb + 2);
             }
 #pragma unroll
@@ -694,7 +799,12 @@ __device__ __forceinline__ void l2_epilogue(const CUtensorMap &tm_out, const L2P
                     release_tbuf(ctrl, b, lane);
             }
         }
-        if (!st.ok || !warp_on) continue;
+        if (!st.ok) break;
+        const Tile t = tile_at(ctrl, st.tc);
+        free_tile(ctrl, st.tc, lane);
+        if (!warp_on) continue;
+        const int cb = t.nb * 2 + h;
+        const bool valid = lrow < t.rows;
         if (q * 32 + 32 <= t.rows) {
             // all 32 rows of the warp valid: two 32 x 64 boxes through shared
             // memory and the copy engine (whole 128-byte row pieces)
@@ -744,6 +854,7 @@ __global__ void __launch_bounds__(kL1Threads, 1)
     const uint32_t base = align1024(raw);
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem_raw + (base - raw) + kL1Stages * kL1StageBytes +
                                           kL1EpiWarps * kL1OutBytes);
+    L1Rows *rows = reinterpret_cast<L1Rows *>(reinterpret_cast<uint8_t *>(ctrl) + kCtrlBytes);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     if (warp == 0 && lane == 0) {
@@ -761,9 +872,12 @@ __global__ void __launch_bounds__(kL1Threads, 1)
         l1_issue(p, r, st);
         if (!st.ok && st.kt > 0)
             drain_wait(smem_u32(&ctrl->tfull[(st.kt - 1) % kL1TBufs]), ((st.kt - 1) / kL1TBufs) & 1, p.err);
+    } else if (warp == kL1LoaderWarp) {
+        l1_load_rows(p, r, rows);
     } else {
-        l1_epilogue<kFast, false>(tm_acts, p, r, st, base + kL1Stages * kL1StageBytes + (warp - kEpiWarp0) * kL1OutBytes,
-                                  nullptr);
+        l1_epilogue<kFast, false, true>(tm_acts, p, r, st,
+                                        base + kL1Stages * kL1StageBytes + (warp - kEpiWarp0) * kL1OutBytes, nullptr,
+                                        rows);
     }
     gemm_teardown(tmem, warp);
 }

@@ -41,17 +41,38 @@ __device__ __forceinline__ Tile decode_tile(int tile, int NB, const int32_t *__r
                                             const int32_t *__restrict__ mblk_expert) {
     const int e = __ldg(mblk_expert + tile / NB);
     const int first = __ldg(mb_prefix + e);
-    const int nmb = __ldg(mb_prefix + e + 1) - first;
     const int off = __ldg(offset + e);
     const int cnt = __ldg(offset + e + 1) - off;
-    return make_tile(tile, NB, e, first, nmb, off, cnt);
+    return make_tile(tile, NB, e, first, (cnt + kBM - 1) / kBM, off, cnt);
+}
+
+// Position p of a CTA's tile walk -> tile index.  Tiles are numbered expert
+// by expert with the one-block experts' tiles last (`singles` of `total`);
+// the walk spreads those evenly among the others (position p takes the next
+// one-block tile when floor((p + 1) s / n) > floor(p s / n)), so that at any
+// time the CTAs streaming once-read weights from HBM are the same share of
+// all CTAs, next to CTAs on weight tiles that several M blocks share.  Each
+// kind keeps its own order, so the N-major walk of a large expert still
+// reaches neighbouring CTAs together.
+__device__ __forceinline__ int tile_at_position(int p, int total, int singles) {
+    const int s0 = (int)((long long)p * singles / total);
+    const int s1 = (int)((long long)(p + 1) * singles / total);
+    return s1 > s0 ? total - singles + s0 : p - s0;
+}
+
+// Tiles of a grouped GEMM with NB column blocks, and how many of them belong
+// to one-block experts (from the block table's last two words).
+__device__ __forceinline__ void tile_counts(const int32_t *mb_prefix, int E, int NB, int &total, int &singles) {
+    const int all = __ldcg(mb_prefix + E);
+    total = all * NB;
+    singles = (all - __ldcg(mb_prefix + E + 1)) * NB;
 }
 
 // The same decode in two steps, for a producer that must not stall on it:
 // begin() loads the tile's expert, finish() (once that has arrived, a stage
 // or so later) the expert's offsets; tile() then needs no load.
 struct TilePrefetch {
-    int tl, e, first, first1, off, off1;
+    int tl, e, first, off, off1;
     // L2-coherent loads: the one-launch forward writes these tables earlier
     // in the same launch
     __device__ __forceinline__ void begin(int tile, int NB, const int32_t *mblk_expert) {
@@ -60,12 +81,11 @@ struct TilePrefetch {
     }
     __device__ __forceinline__ void finish(const int32_t *offset, const int32_t *mb_prefix) {
         first = __ldcg(mb_prefix + e);
-        first1 = __ldcg(mb_prefix + e + 1);
         off = __ldcg(offset + e);
         off1 = __ldcg(offset + e + 1);
     }
     __device__ __forceinline__ Tile tile(int NB) const {
-        return make_tile(tl, NB, e, first, first1 - first, off, off1 - off);
+        return make_tile(tl, NB, e, first, (off1 - off + kBM - 1) / kBM, off, off1 - off);
     }
 };
 

@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int KB = kL1 ? p.H / kBK : p.I / kBK;
     const int brow0 = kL1 ? 2 * p.I : p.H;          // B rows per expert
     const int sf_row_bytes = (kL1 ? p.H : p.I) / 32; // scale bytes per row of A and B
-    const int total = __ldg(p.mb_prefix + p.E) * NB;
+    int total, singles;
+    tile_counts(p.mb_prefix, p.E, NB, total, singles);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            const Tile t = decode_tile(tile_at_position(tile, total, singles), NB, p.offset, p.mb_prefix, p.mblk_expert);
             const uint64_t pol_w = t.nmb > 1 ? pol_shared : pol_once;
             int tok[4] = {0, 0, 0, 0};
             if (kGatherA) {
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            const Tile t = decode_tile(tile_at_position(tile, total, singles), NB, p.offset, p.mb_prefix, p.mblk_expert);
             // row c*32 + lane of the tile: A pool rows c = 0..3, B weight rows
             // c = 0..7 (rows past the expert's last weight row, in a half-empty
             // L2 block, reuse that row: their outputs are masked)
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++tc) {
-            const Tile t = decode_tile(tile, NB, p.offset, p.mb_prefix, p.mblk_expert);
+            const Tile t = decode_tile(tile_at_position(tile, total, singles), NB, p.offset, p.mb_prefix, p.mblk_expert);
             const int b = tc % kAccs;
             if (!mbar_wait(smem_u32(&ctrl->acc_full[b]), (tc / kAccs) & 1, abort_flag, p.err)) {
                 ok = false;

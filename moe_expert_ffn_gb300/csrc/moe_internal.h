@@ -39,7 +39,9 @@ struct AMaps {
 struct DispatchOut {
     int32_t *count;        // [E]
     int32_t *offset;       // [E+1]  exclusive prefix of count
-    int32_t *mb_prefix;    // [E+1]  exclusive prefix of ceil(count/128)
+    int32_t *mb_prefix;    // [E+2]  first 128-row block of each expert (blocks of experts with
+                           //        several blocks first, then one-block experts); [E] all
+                           //        blocks, [E+1] those of the several-block experts
     int32_t *mblk_expert;  // [max M blocks]  expert of each M block
     int32_t *mb2_prefix;   // [E+1]  exclusive prefix of ceil(count/256), or null
     int32_t *mblk2_expert; // [max pair blocks]  expert of each 256-row block

@@ -154,19 +154,27 @@ __device__ __forceinline__ bool dispatch_phase(const int32_t *__restrict__ idx, 
         if (tid == 0) o.offset[E] = P_act;
         // M blocks of 128 rows: the expert's first block and the block -> expert table
         __syncthreads();
-        for (int e = tid; e < E; e += nt) {
-            const int next = (e + 1 < E) ? tot[e + 1] : P_act;
-            hist[e] = (next - tot[e] + kBM - 1) / kBM;   // hist is free again
-        }
-        __syncthreads();
-        const int nmb_total = cta_exclusive_scan(hist, E, scratch);
+        // (experts with several blocks first, then the one-block experts)
         for (int e = tid; e < E; e += nt) {
             const int next = (e + 1 < E) ? tot[e + 1] : P_act;
             const int nmb = (next - tot[e] + kBM - 1) / kBM;
-            o.mb_prefix[e] = hist[e];
-            for (int b = 0; b < nmb; ++b) o.mblk_expert[hist[e] + b] = e;
+            hist[e] = nmb >= 2 ? nmb : 0;   // hist is free again
+            hist[E + e] = nmb == 1 ? 1 : 0;
         }
-        if (tid == 0) o.mb_prefix[E] = nmb_total;
+        __syncthreads();
+        const int multi_total = cta_exclusive_scan(hist, E, scratch);
+        const int single_total = cta_exclusive_scan(hist + E, E, scratch);
+        for (int e = tid; e < E; e += nt) {
+            const int next = (e + 1 < E) ? tot[e + 1] : P_act;
+            const int nmb = (next - tot[e] + kBM - 1) / kBM;
+            const int first = nmb >= 2 ? hist[e] : multi_total + hist[E + e];
+            o.mb_prefix[e] = first;
+            for (int b = 0; b < nmb; ++b) o.mblk_expert[first + b] = e;
+        }
+        if (tid == 0) {
+            o.mb_prefix[E] = multi_total + single_total;
+            o.mb_prefix[E + 1] = multi_total;
+        }
         __syncthreads();
         // restore this CTA's per-warp first slots (pass 2 needs them): recompute
         for (int i = tid; i < nw * E; i += nt) hist[i] = 0;
