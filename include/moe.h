@@ -144,7 +144,11 @@ MOE_API int moe_forward(moe_ctx *ctx, int num_tokens, const void *x, const void 
  * their layer reads inputs already in the symmetric buffer): copies h_x, h_x_sf, h_topk_idx,
  * h_topk_weights into the workspace, runs the forward and copies y back to
  * h_y, then synchronises `stream`.  Host buffers may be pageable or pinned
- * (pinned is faster). */
+ * (pinned is faster).  When h_y is page-locked memory the device can
+ * address (cudaHostAlloc / cudaHostRegister under unified addressing) and
+ * 16-byte aligned, the combine stores y into it directly over the CPU-GPU
+ * link and no copy back is made (environment MOE_HOST_DIRECT=0 turns that
+ * off). */
 MOE_API int moe_forward_host(moe_ctx *ctx, int num_tokens, const void *h_x, const void *h_x_sf,
                      const int32_t *h_topk_idx, const float *h_topk_weights, void *h_y,
                      void *stream);

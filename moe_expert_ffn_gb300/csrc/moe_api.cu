@@ -530,6 +530,25 @@ static int forward_launches(moe_ctx *c, int T, const void *x, const void *x_sf, 
     return MOE_OK;
 }
 
+// Device address of a page-locked host buffer the kernels may store to, or
+// nullptr (pageable memory, no mapping, a misaligned start, or
+// MOE_HOST_DIRECT=0: then the output is staged and copied back).
+static void *host_y_direct(void *h_y) {
+    static const bool off = [] {
+        const char *e = getenv("MOE_HOST_DIRECT");
+        return e && e[0] == '0';
+    }();
+    if (off) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h_y) != cudaSuccess) {
+        cudaGetLastError();   // a pointer the runtime does not know is not an error here
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer || (reinterpret_cast<uintptr_t>(a.devicePointer) & 15))
+        return nullptr;
+    return a.devicePointer;
+}
+
 int moe_forward_host(moe_ctx *c, int T, const void *h_x, const void *h_x_sf,
                      const int32_t *h_topk_idx, const float *h_topk_weights, void *h_y,
                      void *stream) {
@@ -547,12 +566,16 @@ int moe_forward_host(moe_ctx *c, int T, const void *h_x, const void *h_x_sf,
         cudaMemcpyAsync(c->ws + L.st_idx, h_topk_idx, (size_t)T * k * 4, cudaMemcpyHostToDevice, s) ||
         cudaMemcpyAsync(c->ws + L.st_w, h_topk_weights, (size_t)T * k * 4, cudaMemcpyHostToDevice, s))
         return MOE_ERR_CUDA;
+    // A page-locked h_y that the device can address (every pinned allocation
+    // under unified addressing) takes the combine's stores directly, over the
+    // CPU-GPU link, instead of a staging buffer and a copy back.
+    void *y_direct = host_y_direct(h_y);
     int r = moe_forward(c, T, c->ws + L.st_x, c->ws + L.st_xsf, c->w<int32_t>(L.st_idx),
-                        c->w<float>(L.st_w), c->ws + L.st_y, nullptr, stream);
+                        c->w<float>(L.st_w), y_direct ? y_direct : c->ws + L.st_y, nullptr, stream);
     if (r != MOE_OK) return r;
-    if (cudaMemcpyAsync(h_y, c->ws + L.st_y, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s) ||
-        cudaStreamSynchronize(s))
+    if (!y_direct && cudaMemcpyAsync(h_y, c->ws + L.st_y, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s))
         return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s)) return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

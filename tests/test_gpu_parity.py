@@ -328,8 +328,17 @@ def test_forward_host_matches_device(m):
     inp = moe_synth.make_inputs(wl)
     layer, g, y = _run(m, wl, inp)
     pinned = {n: inp[n].pin_memory() for n in ("x", "x_sf", "topk_idx", "topk_weights")}
+    # pinned y: the combine stores into it directly; twice, the second over stale contents
     yh = layer.forward_host(pinned["x"], pinned["x_sf"], pinned["topk_idx"], pinned["topk_weights"])
+    assert yh.is_pinned()
     assert torch.equal(yh, y.cpu())
+    yh.fill_(7.0)
+    layer.forward_host(pinned["x"], pinned["x_sf"], pinned["topk_idx"], pinned["topk_weights"], y=yh)
+    assert torch.equal(yh, y.cpu())
+    # pageable inputs and output: staged in the workspace and copied back
+    yp = torch.full((wl.T, wl.H), 7.0, dtype=torch.bfloat16)
+    layer.forward_host(inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"], y=yp)
+    assert torch.equal(yp, y.cpu())
 
 
 def test_bad_expert_id_is_reported_and_skipped(m, orc):
