@@ -135,7 +135,10 @@ MOE_API int moe_transform_weights(moe_ctx *ctx, const void *w1, const void *w1_s
  *   cumulative_expert_counts  int32 [E] or NULL: the per-expert counts of
  *                 this call are added to it (design §16.1
  *                 "cumulative_local_expert_recv_stats")
- * Asynchronous on `stream`. */
+ * Asynchronous on `stream`.  A call may be captured into a CUDA graph once
+ * the same shape has run eagerly on the context (the first call sets kernel
+ * attributes, once per process); replays read and write the buffers that
+ * were passed at capture, with whatever they hold at replay. */
 MOE_API int moe_forward(moe_ctx *ctx, int num_tokens, const void *x, const void *x_sf,
                 const int32_t *topk_idx, const float *topk_weights, void *y,
                 int32_t *cumulative_expert_counts, void *stream);

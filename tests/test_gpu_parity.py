@@ -341,6 +341,48 @@ def test_forward_host_matches_device(m):
     assert torch.equal(yp, y.cpu())
 
 
+GRAPH_CASES = [
+    moe_synth.custom(T=50, H=384, I=128, E=40, k=3, seed=81, name="graph_sparse"),           # gather4 A
+    moe_synth.custom(T=200, H=512, I=384, E=6, k=4, seed=82, name="graph_pool"),             # pool A
+    moe_synth.custom(T=2048, H=256, I=128, E=64, k=4, seed=83, routing="zipf",
+                     name="graph_multi_cta_dispatch"),                                        # cooperative dispatch
+    moe_synth.custom(T=64, H=256, I=128, E=8, k=2, seed=84, wfmt=1, name="graph_fp4"),
+]
+
+
+@pytest.mark.parametrize("wl", GRAPH_CASES, ids=lambda w: w.name)
+def test_cuda_graph_replay_matches_eager(m, wl):
+    """One forward captured into a CUDA graph and replayed equals the eager
+    forward bit for bit, also after the inputs are rewritten in place (the
+    graph keeps the buffers, not their contents)."""
+    inp = to_dev(moe_synth.make_inputs(wl), DEV)
+    layer = new_layer(m, wl, DEV, wfmt=wl.wfmt)
+    layer.transform_weights(inp["w1"], inp["w1_sf"], inp["w2"], inp["w2_sf"])
+    args = [inp["x"], inp["x_sf"], inp["topk_idx"], inp["topk_weights"]]
+    y_eager = layer.forward(*args).clone()          # also the one-time launch set-up, outside the capture
+    torch.cuda.synchronize()
+    y_graph = torch.empty_like(y_eager)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        layer.forward(*args, y=y_graph)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    assert torch.equal(y_graph, y_eager)
+    # new tokens and routing in the same buffers: replay against eager
+    other = to_dev(moe_synth.make_inputs(wl, weights=False, batch=1), DEV)
+    for a, n in zip(args, ("x", "x_sf", "topk_idx", "topk_weights")):
+        a.copy_(other[n])
+    graph.replay()
+    y2 = layer.forward(*args).clone()
+    torch.cuda.synchronize()
+    assert layer.device_status() == m.MOE_OK
+    assert torch.equal(y_graph, y2)
+    assert not torch.equal(y2, y_eager)
+
+
 def test_bad_expert_id_is_reported_and_skipped(m, orc):
     wl = moe_synth.custom(T=16, H=256, I=128, E=4, k=2, seed=38)
     inp = moe_synth.make_inputs(wl)
