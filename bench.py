@@ -40,6 +40,10 @@ NOMINAL_HBM_GBS = 7900.0     # HBM3e nominal, for context beside the measured co
 # tcgen05 kind::f8f6f4 issue rate per SM per clock.
 CUBLAS_FP8_TFLOPS = 3371.2
 TCGEN05_FP8_MAC_PER_CLK_SM = 8192
+# A read-only HBM stream (16-byte loads over 8 GiB, best of 10, CUDA events):
+# the ceiling of a read-mostly kernel, which the read+write copy peak
+# understates.
+READ_STREAM_GBS = 7049.0
 STAGES = ("dispatch", "l1", "l2", "combine")
 KERNELS = {"dispatch": "dispatch_kernel", "l1": "l1_kernel", "l2": "l2_kernel", "combine": "combine_kernel"}
 KERNELS_FP4 = dict(KERNELS, l1="fp4_gemm_kernel_l1", l2="fp4_gemm_kernel_l2")
@@ -136,13 +140,14 @@ def roofline_for(stage, wm, seconds, peaks, traffic=None):
 
 def alt_fractions(roof, clk):
     """The achieved figure against other denominators, for context: HBM-bound
-    kernels against the nominal bandwidth (the measured copy peak counts the
-    bytes of a read+write copy, so a read-mostly stream can pass 1.0 of it),
+    kernels against the nominal bandwidth and a measured read-only stream
+    (the measured copy peak counts the bytes of a read+write copy, so a
+    read-mostly stream can pass 1.0 of it),
     tensor-bound ones against a measured cuBLAS FP8 GEMM and against the
     tcgen05 FP8 issue rate at the clock sampled during the timed region."""
     a = roof["achieved"]
     if roof["bound"] == "hbm":
-        out = {"vs_nominal_hbm": a / NOMINAL_HBM_GBS}
+        out = {"vs_nominal_hbm": a / NOMINAL_HBM_GBS, "vs_read_stream": a / READ_STREAM_GBS}
     else:
         out = {"vs_cublas_fp8": a / CUBLAS_FP8_TFLOPS}
         if clk and clk.get("sm_mhz"):
